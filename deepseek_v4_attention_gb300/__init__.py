@@ -1,0 +1,236 @@
+"""DeepSeek-V4 attention O-projection on GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in include/dsv4.h (libdsv4.so, built
+in-tree by ``_build.build()``).  The functions below only marshal torch CUDA
+tensors into pointers and sizes; every step of the path runs in the library's
+CUDA kernels.  There is no fallback: if the library is missing or the device
+is not an sm_103 GPU, the calls raise.
+
+    dsv4_inv_rope_fp8_quant  fused inverse RoPE + block-scaled FP8 quantisation
+    dsv4_grouped_wo_a        grouped wo_a block-scaled FP8 GEMM
+    dsv4_o_proj              the whole O-projection (quant -> wo_a -> wo_b)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdsv4.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "dsv4.h")
+
+DSV4_OK = 0
+STATUS = {
+    0: "DSV4_OK", -1: "DSV4_ERR_SHAPE", -2: "DSV4_ERR_NULL", -3: "DSV4_ERR_ALIGN",
+    -4: "DSV4_ERR_UNSUPPORTED", -5: "DSV4_ERR_WORKSPACE", -6: "DSV4_ERR_CUDA",
+    -7: "DSV4_ERR_TIMEOUT", -8: "DSV4_ERR_RANGE",
+}
+_NAME_TO_CODE = {v: k for k, v in STATUS.items()}
+
+
+class DSV4Error(RuntimeError):
+    def __init__(self, rc: int, what: str):
+        super().__init__(f"{what} failed: {STATUS.get(rc, rc)}")
+        self.rc = rc
+        self.name = STATUS.get(rc, str(rc))
+
+
+_lib = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libdsv4.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(or python -m deepseek_v4_attention_gb300._build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.dsv4_inv_rope_fp8_quant.argtypes = [P, P, P, I64, I64, I, I, I, I, I, P, P, P]
+    lib.dsv4_inv_rope_fp8_quant.restype = I
+    lib.dsv4_grouped_wo_a.argtypes = [P, P, I64, I, I, I, P, P, P, P]
+    lib.dsv4_grouped_wo_a.restype = I
+    lib.dsv4_o_proj_workspace_bytes.argtypes = [I64, I, I, I, I]
+    lib.dsv4_o_proj_workspace_bytes.restype = ctypes.c_size_t
+    lib.dsv4_o_proj.argtypes = [P, P, P, I64, I64, I, I, I, I, I, I, I, P, P, P, P, P, P,
+                                ctypes.c_size_t, P]
+    lib.dsv4_o_proj.restype = I
+    lib.dsv4_status_string.argtypes = [I]
+    lib.dsv4_status_string.restype = ctypes.c_char_p
+    lib.dsv4_device_status.argtypes = [P, I]
+    lib.dsv4_device_status.restype = I
+    lib.dsv4_last_launch_count.argtypes = []
+    lib.dsv4_last_launch_count.restype = I
+    _lib = lib
+    return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/dsv4.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"\b(dsv4_\w+)\s*\(", text)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _check(rc: int, what: str):
+    if rc != DSV4_OK:
+        raise DSV4Error(rc, what)
+
+
+def _cuda(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def tma_aligned_tokens(T: int) -> int:
+    return (T + 3) // 4 * 4
+
+
+_FP8 = (torch.float8_e4m3fn, torch.uint8)
+_SCALE8 = (torch.uint8, torch.float8_e8m0fnu) if hasattr(torch, "float8_e8m0fnu") else (torch.uint8,)
+
+
+def dsv4_inv_rope_fp8_quant(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                            n_groups: int, heads_per_group: int, nope_dim: int = 448,
+                            rope_dim: int = 64, quant_group_size: int = 128, *,
+                            out_fp8: torch.Tensor | None = None,
+                            out_scale: torch.Tensor | None = None, stream=None):
+    """Returns (o_fp8 [T, G, D] float8_e4m3fn with strides (D, T*D, 1),
+    o_scale [T, G, PK] int32 with strides (1, PK*T_al, T_al))."""
+    lib = load_library()
+    _cuda(o, "o", torch.bfloat16)
+    _cuda(positions, "positions", torch.int64)
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    if o.dim() != 3 or not o.is_contiguous():
+        raise ValueError("o must be a contiguous [T, H, head_dim] tensor")
+    if not positions.is_contiguous() or not cos_sin_cache.is_contiguous():
+        raise ValueError("positions and cos_sin_cache must be contiguous")
+    T, H, hd = o.shape
+    if H != n_groups * heads_per_group:
+        raise DSV4Error(-1, "dsv4_inv_rope_fp8_quant (num_heads != n_groups * heads_per_group)")
+    if hd != nope_dim + rope_dim or cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != rope_dim:
+        raise DSV4Error(-1, "dsv4_inv_rope_fp8_quant (head_dim / cache shape)")
+    if positions.numel() != T:
+        raise DSV4Error(-1, "dsv4_inv_rope_fp8_quant (positions length)")
+    D = heads_per_group * hd
+    PK = (D // quant_group_size + 3) // 4 if quant_group_size > 0 else 0
+    T_al = tma_aligned_tokens(T)
+    if out_fp8 is None:
+        out_fp8 = torch.empty((n_groups, T, D), dtype=torch.float8_e4m3fn, device=o.device)
+    if out_scale is None:
+        out_scale = torch.empty((n_groups, PK, T_al), dtype=torch.int32, device=o.device)
+    rc = lib.dsv4_inv_rope_fp8_quant(o.data_ptr(), positions.data_ptr(), cos_sin_cache.data_ptr(),
+                                     T, cos_sin_cache.shape[0], n_groups, heads_per_group,
+                                     nope_dim, rope_dim, quant_group_size, out_fp8.data_ptr(),
+                                     out_scale.data_ptr(), _stream(stream))
+    _check(rc, "dsv4_inv_rope_fp8_quant")
+    return out_fp8.transpose(0, 1), out_scale.permute(2, 0, 1)[:T]
+
+
+def dsv4_grouped_wo_a(x_fp8: torch.Tensor, x_scale: torch.Tensor, w_fp8: torch.Tensor,
+                      w_scale: torch.Tensor, n_groups: int, o_lora_rank: int, *,
+                      z: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """x_fp8: the [T, G, D] view (strides (D, T*D, 1)) the quantiser returns;
+    x_scale: the matching [T, G, PK] view.  Returns bf16 z [T, G, R]."""
+    lib = load_library()
+    _cuda(x_fp8, "x_fp8", _FP8)
+    _cuda(x_scale, "x_scale", torch.int32)
+    _cuda(w_fp8, "w_fp8", _FP8)
+    _cuda(w_scale, "w_scale", _SCALE8)
+    T, G, D = x_fp8.shape
+    if G != n_groups or x_fp8.stride() != (D, T * D, 1):
+        raise ValueError("x_fp8 must be the [T, G, D] view of a physical [G, T, D] buffer")
+    PK = (D // 128 + 3) // 4
+    T_al = tma_aligned_tokens(T)
+    if T > 0 and (tuple(x_scale.shape) != (T, G, PK) or x_scale.stride() != (1, PK * T_al, T_al)):
+        raise ValueError("x_scale must be the [T, G, PK] view of a physical [G, PK, T_al] buffer")
+    if tuple(w_fp8.shape) != (G * o_lora_rank, D) or not w_fp8.is_contiguous():
+        raise ValueError("w_fp8 must be a contiguous [G*R, D] tensor")
+    if tuple(w_scale.shape) != (G * o_lora_rank // 128, D // 128) or not w_scale.is_contiguous():
+        raise ValueError("w_scale must be a contiguous [G*R/128, D/128] tensor")
+    if z is None:
+        z = torch.empty((T, G, o_lora_rank), dtype=torch.bfloat16, device=x_fp8.device)
+    rc = lib.dsv4_grouped_wo_a(x_fp8.data_ptr(), x_scale.data_ptr(), T, G, D, o_lora_rank,
+                               w_fp8.data_ptr(), w_scale.data_ptr(), z.data_ptr(), _stream(stream))
+    _check(rc, "dsv4_grouped_wo_a")
+    return z
+
+
+def dsv4_o_proj_workspace_bytes(num_tokens: int, n_groups: int, heads_per_group: int,
+                                head_dim: int, o_lora_rank: int) -> int:
+    return int(load_library().dsv4_o_proj_workspace_bytes(num_tokens, n_groups, heads_per_group,
+                                                          head_dim, o_lora_rank))
+
+
+def dsv4_o_proj(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                wo_a: torch.Tensor, wo_a_scale: torch.Tensor, wo_b: torch.Tensor,
+                wo_b_scale: torch.Tensor, *, n_groups: int, heads_per_group: int,
+                o_lora_rank: int, nope_dim: int = 448, rope_dim: int = 64,
+                quant_group_size: int = 128, out: torch.Tensor | None = None,
+                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The whole O-projection: returns bf16 out [T, hidden]."""
+    lib = load_library()
+    _cuda(o, "o", torch.bfloat16)
+    _cuda(positions, "positions", torch.int64)
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    for t, n in ((wo_a, "wo_a"), (wo_b, "wo_b")):
+        _cuda(t, n, _FP8)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for t, n in ((wo_a_scale, "wo_a_scale"), (wo_b_scale, "wo_b_scale")):
+        _cuda(t, n, _SCALE8)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if o.dim() != 3 or not o.is_contiguous():
+        raise ValueError("o must be a contiguous [T, H, head_dim] tensor")
+    T, H, hd = o.shape
+    if H != n_groups * heads_per_group or positions.numel() != T:
+        raise DSV4Error(-1, "dsv4_o_proj (head count / positions)")
+    hidden = wo_b.shape[0]
+    C = n_groups * o_lora_rank
+    D = heads_per_group * hd
+    if tuple(wo_a.shape) != (C, D) or tuple(wo_b.shape) != (hidden, C):
+        raise ValueError("weight shapes must be wo_a [G*R, D] and wo_b [hidden, G*R]")
+    if tuple(wo_a_scale.shape) != (C // 128, D // 128) or \
+            tuple(wo_b_scale.shape) != (hidden // 128, C // 128):
+        raise ValueError("weight scales must be [rows/128, cols/128]")
+    need = dsv4_o_proj_workspace_bytes(T, n_groups, heads_per_group, hd, o_lora_rank)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=o.device)
+    if out is None:
+        out = torch.empty((T, hidden), dtype=torch.bfloat16, device=o.device)
+    rc = lib.dsv4_o_proj(o.data_ptr(), positions.data_ptr(), cos_sin_cache.data_ptr(),
+                         cos_sin_cache.shape[0], T, n_groups, heads_per_group, nope_dim, rope_dim,
+                         quant_group_size, o_lora_rank, hidden, wo_a.data_ptr(),
+                         wo_a_scale.data_ptr(), wo_b.data_ptr(), wo_b_scale.data_ptr(),
+                         out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check(rc, "dsv4_o_proj")
+    return out
+
+
+def dsv4_device_status(clear: bool = True, stream=None) -> int:
+    """Device status word (0 = OK, else a negative dsv4_status); synchronises the stream."""
+    return int(load_library().dsv4_device_status(_stream(stream), 1 if clear else 0))
+
+
+def dsv4_status_string(status: int) -> str:
+    return load_library().dsv4_status_string(status).decode()
+
+
+def dsv4_last_launch_count() -> int:
+    return int(load_library().dsv4_last_launch_count())

@@ -1,0 +1,283 @@
+// dsv4_api.cu -- the C ABI (include/dsv4.h): host-side validation, workspace
+// carving and launches.  Nothing here allocates device memory or synchronises
+// a stream, except dsv4_device_status(), whose job is to read the status word.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/dsv4.h"
+#include "dsv4_internal.h"
+
+namespace dsv4 {
+
+// The device status word: one per device (a module-scope variable, so it exists
+// on every device that loads this library without any run-time allocation).
+__device__ int g_status_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::once_flag g_device_once[kMaxDevices];
+int g_device_rc[kMaxDevices];
+
+thread_local int t_last_launches = 0;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+int64_t tma_aligned_tokens(int64_t T) { return (T + 3) / 4 * 4; }
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+int check_quant_shapes(int64_t T, int64_t max_pos, int n_groups, int hpg, int nope, int rope,
+                       int qgs) {
+  if (T < 0 || n_groups <= 0 || hpg <= 0 || qgs <= 0 || nope < 0 || rope < 0)
+    return DSV4_ERR_SHAPE;
+  const int head_dim = nope + rope;
+  // the asserts of fused_inv_rope_fp8_quant (H == G * hpg holds by construction here)
+  if (head_dim % qgs != 0) return DSV4_ERR_SHAPE;
+  if (nope % qgs != qgs - rope) return DSV4_ERR_SHAPE;
+  if (rope % 2 != 0) return DSV4_ERR_SHAPE;
+  if (max_pos <= 0) return DSV4_ERR_SHAPE;
+  if (static_cast<int64_t>(n_groups) * hpg > (1 << 20)) return DSV4_ERR_SHAPE;
+  return DSV4_OK;
+}
+
+int check_quant_supported(int nope, int rope, int qgs) {
+  if (nope != 448 || rope != 64 || qgs != 128) return DSV4_ERR_UNSUPPORTED;
+  return DSV4_OK;
+}
+
+}  // namespace
+
+int get_device_info(DeviceInfo* out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSV4_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DSV4_ERR_UNSUPPORTED;
+  std::call_once(g_device_once[dev], [dev] {
+    DeviceInfo d;
+    d.device = dev;
+    int v = 0;
+    g_device_rc[dev] = DSV4_OK;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      g_device_rc[dev] = DSV4_ERR_CUDA;
+      return;
+    }
+    d.max_smem_optin = static_cast<size_t>(v);
+    if (d.cc_major != 10 || d.cc_minor != 3) {  // this build carries sm_103a code only
+      g_device_rc[dev] = DSV4_ERR_UNSUPPORTED;
+      return;
+    }
+    void* sym = nullptr;
+    if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess) {
+      g_device_rc[dev] = DSV4_ERR_CUDA;
+      return;
+    }
+    d.status = static_cast<int*>(sym);
+    g_devices[dev] = d;
+  });
+  if (g_device_rc[dev] != DSV4_OK) return g_device_rc[dev];
+  *out = g_devices[dev];
+  return DSV4_OK;
+}
+
+}  // namespace dsv4
+
+using namespace dsv4;
+
+extern "C" {
+
+const char* dsv4_status_string(int status) {
+  switch (status) {
+    case DSV4_OK: return "DSV4_OK";
+    case DSV4_ERR_SHAPE: return "DSV4_ERR_SHAPE: invalid sizes";
+    case DSV4_ERR_NULL: return "DSV4_ERR_NULL: null pointer";
+    case DSV4_ERR_ALIGN: return "DSV4_ERR_ALIGN: misaligned pointer";
+    case DSV4_ERR_UNSUPPORTED: return "DSV4_ERR_UNSUPPORTED: device or parameter not supported";
+    case DSV4_ERR_WORKSPACE: return "DSV4_ERR_WORKSPACE: workspace missing or too small";
+    case DSV4_ERR_CUDA: return "DSV4_ERR_CUDA: CUDA call failed";
+    case DSV4_ERR_TIMEOUT: return "DSV4_ERR_TIMEOUT: a kernel pipeline wait timed out";
+    case DSV4_ERR_RANGE: return "DSV4_ERR_RANGE: position outside [0, max_pos)";
+    default: return "unknown dsv4 status";
+  }
+}
+
+int dsv4_last_launch_count(void) { return t_last_launches; }
+
+int dsv4_inv_rope_fp8_quant(const void* o, const int64_t* positions, const float* cos_sin_cache,
+                            int64_t num_tokens, int64_t max_pos, int n_groups,
+                            int heads_per_group, int nope_dim, int rope_dim,
+                            int quant_group_size, void* out_fp8, int32_t* out_scale,
+                            void* stream) {
+  t_last_launches = 0;
+  int rc = check_quant_shapes(num_tokens, max_pos, n_groups, heads_per_group, nope_dim, rope_dim,
+                              quant_group_size);
+  if (rc != DSV4_OK) return rc;
+  if ((rc = check_quant_supported(nope_dim, rope_dim, quant_group_size)) != DSV4_OK) return rc;
+  if (num_tokens == 0) return DSV4_OK;
+  if (!o || !positions || !cos_sin_cache || !out_fp8 || !out_scale) return DSV4_ERR_NULL;
+  if (!aligned16(o) || !aligned16(positions) || !aligned16(cos_sin_cache) ||
+      !aligned16(out_fp8) || !aligned16(out_scale))
+    return DSV4_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = get_device_info(&dev)) != DSV4_OK) return rc;
+  rc = launch_inv_rope_fp8_quant(o, positions, cos_sin_cache, num_tokens, max_pos, n_groups,
+                                 heads_per_group, out_fp8, out_scale,
+                                 static_cast<cudaStream_t>(stream), dev);
+  if (rc == DSV4_OK) t_last_launches = 1;
+  return rc;
+}
+
+int dsv4_grouped_wo_a(const void* x_fp8, const int32_t* x_scale, int64_t num_tokens,
+                      int n_groups, int group_dim, int o_lora_rank, const void* w_fp8,
+                      const uint8_t* w_scale, void* z, void* stream) {
+  t_last_launches = 0;
+  if (num_tokens < 0 || n_groups <= 0 || group_dim <= 0 || o_lora_rank <= 0 ||
+      group_dim % 128 != 0 || o_lora_rank % 128 != 0)
+    return DSV4_ERR_SHAPE;
+  if (num_tokens == 0) return DSV4_OK;
+  if (!x_fp8 || !x_scale || !w_fp8 || !w_scale || !z) return DSV4_ERR_NULL;
+  if (!aligned16(x_fp8) || !aligned16(x_scale) || !aligned16(w_fp8) || !aligned16(z))
+    return DSV4_ERR_ALIGN;
+  if (num_tokens > (int64_t(1) << 31) - 128) return DSV4_ERR_SHAPE;
+  DeviceInfo dev;
+  int rc = get_device_info(&dev);
+  if (rc != DSV4_OK) return rc;
+  GemmProblem p;
+  p.T = num_tokens;
+  p.G = n_groups;
+  p.N = o_lora_rank;
+  p.K = group_dim;
+  p.a = x_fp8;
+  p.a_scale = x_scale;
+  p.b = w_fp8;
+  p.b_scale = w_scale;
+  p.epilogue = kEpiBf16;
+  p.out_bf16 = z;
+  rc = launch_block_scaled_gemm(p, static_cast<cudaStream_t>(stream), dev);
+  if (rc == DSV4_OK) t_last_launches = 1;
+  return rc;
+}
+
+size_t dsv4_o_proj_workspace_bytes(int64_t num_tokens, int n_groups, int heads_per_group,
+                                   int head_dim, int o_lora_rank) {
+  if (num_tokens < 0 || n_groups <= 0 || heads_per_group <= 0 || head_dim <= 0 ||
+      head_dim % 128 != 0 || o_lora_rank <= 0 || o_lora_rank % 128 != 0)
+    return 0;
+  const int64_t T = num_tokens;
+  const int64_t T_al = tma_aligned_tokens(T);
+  const int64_t D = static_cast<int64_t>(heads_per_group) * head_dim;
+  const int64_t PK = (D / 128 + 3) / 4;
+  const int64_t C = static_cast<int64_t>(n_groups) * o_lora_rank;
+  const int64_t PKC = (C / 128 + 3) / 4;
+  size_t bytes = 0;
+  bytes += round256(static_cast<size_t>(n_groups) * T * D);        // x codes
+  bytes += round256(static_cast<size_t>(n_groups) * PK * T_al * 4); // x scales
+  bytes += round256(static_cast<size_t>(T) * C);                    // zq codes
+  bytes += round256(static_cast<size_t>(PKC) * T_al * 4);           // zq scales
+  return bytes == 0 ? 256 : bytes;
+}
+
+int dsv4_o_proj(const void* o, const int64_t* positions, const float* cos_sin_cache,
+                int64_t max_pos, int64_t num_tokens, int n_groups, int heads_per_group,
+                int nope_dim, int rope_dim, int quant_group_size, int o_lora_rank, int hidden,
+                const void* wo_a_fp8, const uint8_t* wo_a_scale, const void* wo_b_fp8,
+                const uint8_t* wo_b_scale, void* out, void* workspace, size_t workspace_bytes,
+                void* stream) {
+  t_last_launches = 0;
+  int rc = check_quant_shapes(num_tokens, max_pos, n_groups, heads_per_group, nope_dim, rope_dim,
+                              quant_group_size);
+  if (rc != DSV4_OK) return rc;
+  if (o_lora_rank <= 0 || o_lora_rank % 128 != 0 || hidden <= 0 || hidden % 128 != 0)
+    return DSV4_ERR_SHAPE;
+  if ((rc = check_quant_supported(nope_dim, rope_dim, quant_group_size)) != DSV4_OK) return rc;
+  if (num_tokens == 0) return DSV4_OK;
+  if (num_tokens > (int64_t(1) << 31) - 128) return DSV4_ERR_SHAPE;
+  if (!o || !positions || !cos_sin_cache || !wo_a_fp8 || !wo_a_scale || !wo_b_fp8 ||
+      !wo_b_scale || !out)
+    return DSV4_ERR_NULL;
+  if (!aligned16(o) || !aligned16(positions) || !aligned16(cos_sin_cache) ||
+      !aligned16(wo_a_fp8) || !aligned16(wo_b_fp8) || !aligned16(out))
+    return DSV4_ERR_ALIGN;
+  const int head_dim = nope_dim + rope_dim;
+  const size_t need =
+      dsv4_o_proj_workspace_bytes(num_tokens, n_groups, heads_per_group, head_dim, o_lora_rank);
+  if (!workspace || workspace_bytes < need) return DSV4_ERR_WORKSPACE;
+  if (!aligned256(workspace)) return DSV4_ERR_ALIGN;
+
+  DeviceInfo dev;
+  if ((rc = get_device_info(&dev)) != DSV4_OK) return rc;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  const int64_t T = num_tokens;
+  const int64_t T_al = tma_aligned_tokens(T);
+  const int64_t D = static_cast<int64_t>(heads_per_group) * head_dim;
+  const int64_t PK = (D / 128 + 3) / 4;
+  const int64_t C = static_cast<int64_t>(n_groups) * o_lora_rank;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* x = ws;
+  ws += round256(static_cast<size_t>(n_groups) * T * D);
+  int32_t* xs = reinterpret_cast<int32_t*>(ws);
+  ws += round256(static_cast<size_t>(n_groups) * PK * T_al * 4);
+  uint8_t* zq = ws;
+  ws += round256(static_cast<size_t>(T) * C);
+  int32_t* zs = reinterpret_cast<int32_t*>(ws);
+
+  rc = launch_inv_rope_fp8_quant(o, positions, cos_sin_cache, T, max_pos, n_groups,
+                                 heads_per_group, x, xs, s, dev);
+  if (rc != DSV4_OK) return rc;
+
+  GemmProblem a;
+  a.T = T;
+  a.G = n_groups;
+  a.N = o_lora_rank;
+  a.K = static_cast<int>(D);
+  a.a = x;
+  a.a_scale = xs;
+  a.b = wo_a_fp8;
+  a.b_scale = wo_a_scale;
+  a.epilogue = kEpiQuant;
+  a.q_out = zq;
+  a.q_scale = zs;
+  if ((rc = launch_block_scaled_gemm(a, s, dev)) != DSV4_OK) return rc;
+
+  GemmProblem b;
+  b.T = T;
+  b.G = 1;
+  b.N = hidden;
+  b.K = static_cast<int>(C);
+  b.a = zq;
+  b.a_scale = zs;
+  b.b = wo_b_fp8;
+  b.b_scale = wo_b_scale;
+  b.epilogue = kEpiBf16;
+  b.out_bf16 = out;
+  if ((rc = launch_block_scaled_gemm(b, s, dev)) != DSV4_OK) return rc;
+  t_last_launches = 3;
+  return DSV4_OK;
+}
+
+int dsv4_device_status(void* stream, int clear) {
+  DeviceInfo dev;
+  int rc = get_device_info(&dev);
+  if (rc != DSV4_OK) return rc;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSV4_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, dev.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DSV4_ERR_CUDA;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpy(dev.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return DSV4_ERR_CUDA;
+  }
+  return v;
+}
+
+}  // extern "C"

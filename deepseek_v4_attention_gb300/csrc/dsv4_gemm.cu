@@ -1,0 +1,485 @@
+// dsv4_gemm.cu -- block-scaled FP8 GEMM on the 5th-generation tensor cores
+// (tcgen05, kind::mxf8f6f4 with UE8M0 block scales), for both projections of
+// the O-projection:
+//   - grouped wo_a (vLLM docs, grouped_wo_a: group g meets rows g*R:(g+1)*R;
+//     o_proj page, fp8_einsum("bhr,hdr->bhd") with recipe (1, 1, 128)),
+//   - dense wo_b over z.flatten(1) (the same kernel with G = 1).
+//
+//   C[t, g*N + n] = sum_k A[g][t][k] 2^ea[g][t][k/128] * B[g*N+n][k] 2^eb[(g*N+n)/128][k/128]
+//
+// Persistent, warp-specialised CTA of 192 threads, one CTA per SM:
+//   warp 0     TMA producer: A tile (128 tokens x 128 k, 128B swizzle),
+//              B tile (128 rows x 128 k), the A scale words of the k-block
+//              (512 B, MN-major as the quantiser writes them); the B scales
+//              are one UE8M0 byte per (128-row block, k-block), expanded here
+//              into the 128-row scale-factor tile.
+//   warp 1     allocates TMEM; one lane issues tcgen05.cp (scale factors ->
+//              TMEM) and 4 tcgen05.mma (K = 32 each) per k-block; the whole
+//              warp first reorders the A scale words into the 32 x 16-byte
+//              layout that tcgen05.cp.32x128b.warpx4 expects.
+//   warps 2-5  epilogue: tcgen05.ld the 128 x 128 fp32 accumulator (each
+//              thread one row), then bf16 stores or the fused per-128 FP8
+//              re-quantisation.
+// TMEM: two 128-column accumulators (the epilogue of tile i overlaps the
+// MMAs of tile i+1) + 8 scale-factor columns per pipeline stage.
+//
+// Scale factors and the K = 128 blocks: the hardware applies one UE8M0 scale
+// per 32 k (scale_vec::1X).  A 128-wide k-block is issued as four K = 32 MMAs
+// that all select the same scale byte, which is exact: the four products are
+// scaled by the same power of two.  The byte is chosen with the
+// scale-factor-id field of the instruction descriptor: the 4 blocks of a
+// packed int32 are bytes 0..3 of one TMEM column word.
+#include <cuda/std/cstdint>
+
+#include "dsv4_device.cuh"
+#include "dsv4_internal.h"
+
+namespace dsv4 {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kBK = 128;
+constexpr int kStages = 6;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = 2 * kBN;          // two accumulators
+constexpr int kSfCol0 = kAccCols;          // scale factors after the accumulators
+constexpr int kSfColsPerStage = 8;         // 4 for A (128 rows), 4 for B (128 rows)
+static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+
+constexpr uint32_t kABytes = kBM * kBK;    // 16 KiB
+constexpr uint32_t kBBytes = kBN * kBK;    // 16 KiB
+constexpr uint32_t kSfaBytes = kBM * 4;    // 512 B
+constexpr uint32_t kSfbBytes = kBN * 4;    // 512 B
+
+struct SmemPlan {
+  static constexpr uint32_t a = 0;
+  static constexpr uint32_t b = a + kStages * kABytes;
+  static constexpr uint32_t sfa = b + kStages * kBBytes;
+  static constexpr uint32_t sfb = sfa + kStages * kSfaBytes;
+  static constexpr uint32_t bars = sfb + kStages * kSfbBytes;
+  // full[kStages], empty[kStages], tmem_full[2], tmem_empty[2], drain
+  static constexpr uint32_t n_bars = 2 * kStages + 5;
+  static constexpr uint32_t misc = bars + n_bars * 8;  // tmem base, abort flag
+  static constexpr uint32_t total = misc + 16;
+};
+constexpr uint32_t kSmemBytes = SmemPlan::total + 1024;  // + alignment slack
+
+struct Params {
+  int64_t T;
+  int G, N, K;
+  int m_tiles, n_tiles, num_tiles, k_blocks;
+  int64_t t_al;
+  const uint8_t* b_scale;
+  int b_scale_ld;          // K / 128
+  __nv_bfloat16* out;      // [T][G*N] or null
+  uint8_t* q_out;          // [T][G*N]
+  int32_t* q_scale;        // [ceil(G*N/512)][t_al]
+  int* status;             // device status word
+};
+
+__device__ __forceinline__ void tile_coords(const Params& p, int tile, int& g, int& n_blk,
+                                            int& m_blk) {
+  m_blk = tile % p.m_tiles;
+  const int rest = tile / p.m_tiles;
+  n_blk = rest % p.n_tiles;
+  g = rest / p.n_tiles;
+}
+
+// Packed scale word of weight row block `rb` for k-blocks 4j..4j+3 (bytes
+// beyond the last k-block are 0).
+__device__ __forceinline__ uint32_t b_scale_word(const Params& p, int rb, int j) {
+  const uint8_t* row = p.b_scale + static_cast<int64_t>(rb) * p.b_scale_ld;
+  uint32_t w = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int kb = 4 * j + b;
+    if (kb < p.k_blocks) w |= static_cast<uint32_t>(__ldg(row + kb)) << (8 * b);
+  }
+  return w;
+}
+
+template <int kEpi>
+__global__ void __launch_bounds__(kThreads, 1)
+    block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                             const __grid_constant__ CUtensorMap tm_b,
+                             const __grid_constant__ CUtensorMap tm_sfa, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128B-swizzled operand tiles
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemPlan::bars);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tmem_full = bars + 2 * kStages;
+  uint64_t* tmem_empty = bars + 2 * kStages + 2;
+  uint64_t* drain = bars + 2 * kStages + 4;
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + SmemPlan::misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemPlan::misc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tmem_full[a], 1);
+      mbar_init(&tmem_empty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&tm_sfa);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_base_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0;
+    bool issued[kStages];
+    uint32_t issued_parity[kStages];
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) { issued[s] = false; issued_parity[s] = 0; }
+    const int packs = (p.k_blocks + 3) / 4;
+    bool ok = true;
+    // weight-scale words of the first tile, loaded ahead (lane j holds packs j, j+32, ...)
+    uint32_t wnext[4] = {0, 0, 0, 0};
+    if (blockIdx.x < p.num_tiles) {
+      int g, nb, mb;
+      tile_coords(p, blockIdx.x, g, nb, mb);
+      const int rb = (g * p.N + nb * kBN) / 128;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (lane + 32 * i < packs) wnext[i] = b_scale_word(p, rb, lane + 32 * i);
+    }
+    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      int g, n_blk, m_blk;
+      tile_coords(p, tile, g, n_blk, m_blk);
+      uint32_t wcur[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) wcur[i] = wnext[i];
+      const int next = tile + gridDim.x;
+      if (next < p.num_tiles) {
+        int g2, nb2, mb2;
+        tile_coords(p, next, g2, nb2, mb2);
+        const int rb2 = (g2 * p.N + nb2 * kBN) / 128;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          wnext[i] = (lane + 32 * i < packs) ? b_scale_word(p, rb2, lane + 32 * i) : 0u;
+      }
+      const int m0 = m_blk * kBM;
+      const int brow = g * p.N + n_blk * kBN;
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        // B scale-factor tile: 128 rows share the byte of their 128-row block
+        const int j = kb >> 2;
+        const uint32_t src = (j < 32) ? wcur[0] : (j < 64) ? wcur[1] : (j < 96) ? wcur[2] : wcur[3];
+        const uint32_t word = __shfl_sync(0xFFFFFFFFu, src, j & 31);
+        uint4* sfb = reinterpret_cast<uint4*>(smem + SmemPlan::sfb + stage * kSfbBytes);
+        sfb[lane] = make_uint4(word, word, word, word);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + kSfaBytes);
+          tma_load_3d(smem + SmemPlan::a + stage * kABytes, &tm_a, &full[stage], kb * kBK, m0, g);
+          tma_load_2d(smem + SmemPlan::b + stage * kBBytes, &tm_b, &full[stage], kb * kBK, brow);
+          tma_load_3d(smem + SmemPlan::sfa + stage * kSfaBytes, &tm_sfa, &full[stage], m0, j, g);
+        }
+        issued[stage] = true;
+        issued_parity[stage] = phase;
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok && lane == 0) {
+      // drain: let every copy this warp issued land before the CTA exits
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s]) mbar_wait_drain(&full[s], issued_parity[s]);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      if (!mbar_wait_warp(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        if (!mbar_wait_warp(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        // reorder the 128 A scale words: row m = 32 i + r goes to word 4 r + i
+        uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + SmemPlan::sfa + stage * kSfaBytes);
+        uint32_t v0 = sfa[lane], v1 = sfa[32 + lane], v2 = sfa[64 + lane], v3 = sfa[96 + lane];
+        __syncwarp();
+        reinterpret_cast<uint4*>(sfa)[lane] = make_uint4(v0, v1, v2, v3);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t sf_col =
+              tmem_base + static_cast<uint32_t>(kSfCol0 + stage * kSfColsPerStage);
+          const uint32_t sfa_addr = smem_addr(sfa);
+          const uint32_t sfb_addr = smem_addr(smem + SmemPlan::sfb + stage * kSfbBytes);
+          tmem_cp_32x128b_x4(sf_col, smem_desc(sfa_addr, 0, 128, 0));
+          tmem_cp_32x128b_x4(sf_col + 4, smem_desc(sfb_addr, 0, 128, 0));
+          const uint32_t a_addr = smem_addr(smem + SmemPlan::a + stage * kABytes);
+          const uint32_t b_addr = smem_addr(smem + SmemPlan::b + stage * kBBytes);
+          const uint32_t id = static_cast<uint32_t>(kb & 3);
+          const uint32_t idesc = mxf8_idesc(kBM, kBN, id, id);
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k) {
+            const uint64_t ad = smem_desc(a_addr + 32u * k, 16, 1024, 2);
+            const uint64_t bd = smem_desc(b_addr + 32u * k, 16, 1024, 2);
+            mma_mxf8(d_tmem, ad, bd, idesc, sf_col, sf_col + 4, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&tmem_full[acc]);
+      __syncwarp();
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (*abort_flag && lane == 0) {
+      // let every MMA / copy this thread issued finish before TMEM is freed
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row = quarter * 32 + lane;
+    const int64_t ld = static_cast<int64_t>(p.G) * p.N;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      int g, n_blk, m_blk;
+      tile_coords(p, tile, g, n_blk, m_blk);
+      if (!mbar_wait_warp(&tmem_full[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int64_t t = static_cast<int64_t>(m_blk) * kBM + row;
+      const bool live = t < p.T;
+      const int64_t col0 = static_cast<int64_t>(g) * p.N + static_cast<int64_t>(n_blk) * kBN;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * kBN);
+      if constexpr (kEpi == kEpiBf16) {
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32cols(taddr + 32u * c, r);
+          tmem_ld_wait();
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + t * ld + col0 + 32 * c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * i]),
+                                                               __uint_as_float(r[8 * v + 2 * i + 1]));
+                w[i] = *reinterpret_cast<const uint32_t*>(&h);
+              }
+              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      } else {
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_32cols(taddr + 32u * c, r[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tmem_empty[acc]);  // accumulator is in registers now
+        // z is a bf16 tensor: round first, then quantise the rounded values
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float zr = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[c][i])));
+            r[c][i] = __float_as_uint(zr);
+            amax = fmaxf(amax, fabsf(zr));
+          }
+        if (live) {
+          if (p.out != nullptr) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out + t * ld + col0 + 32 * c);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  w[i] = (r[c][8 * v + 2 * i] >> 16) | (r[c][8 * v + 2 * i + 1] & 0xFFFF0000u);
+                dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          }
+          const int e = ue8m0_exponent(amax);
+          const float inv = exp2_neg(e);
+          uint4* qdst = reinterpret_cast<uint4*>(p.q_out + t * ld + col0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int b = 16 * v + 4 * i;
+                w[i] = static_cast<uint32_t>(e4m3x2(__uint_as_float(r[c][b]) * inv,
+                                                    __uint_as_float(r[c][b + 1]) * inv)) |
+                       (static_cast<uint32_t>(e4m3x2(__uint_as_float(r[c][b + 2]) * inv,
+                                                     __uint_as_float(r[c][b + 3]) * inv))
+                        << 16);
+              }
+              qdst[2 * c + v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          const int64_t blk = col0 / 128;  // 128-column block of the flattened row
+          uint8_t* sbytes = reinterpret_cast<uint8_t*>(p.q_scale);
+          sbytes[((blk >> 2) * p.t_al + t) * 4 + (blk & 3)] = static_cast<uint8_t>(e + 127);
+        }
+      }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------- host side --
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+            const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,
+            CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t elem_strides[3] = {1, 1, 1};
+  return fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides_bytes,
+            box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int kEpi>
+int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
+  static int configured_for[64] = {0};
+  if (dev.device < 0 || dev.device >= 64) return DSV4_ERR_UNSUPPORTED;
+  if (!configured_for[dev.device]) {
+    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kEpi>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+      return DSV4_ERR_CUDA;
+    configured_for[dev.device] = 1;
+  }
+  const int64_t T = q.T;
+  const int64_t t_al = (T + 3) / 4 * 4;
+  const int packs = (q.K / 128 + 3) / 4;
+
+  CUtensorMap tm_a, tm_b, tm_sfa;
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(q.K), static_cast<cuuint64_t>(T),
+                          static_cast<cuuint64_t>(q.G)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.K), static_cast<cuuint64_t>(T * q.K)};
+    cuuint32_t box[3] = {kBK, kBM, 1};
+    if (!encode(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q.a, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+      return DSV4_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(q.K),
+                          static_cast<cuuint64_t>(static_cast<int64_t>(q.G) * q.N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(q.K)};
+    cuuint32_t box[2] = {kBK, kBN};
+    if (!encode(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q.b, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+      return DSV4_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(packs),
+                          static_cast<cuuint64_t>(q.G)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(t_al * 4),
+                             static_cast<cuuint64_t>(t_al * 4 * packs)};
+    cuuint32_t box[3] = {kBM, 1, 1};
+    if (!encode(&tm_sfa, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, q.a_scale, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+      return DSV4_ERR_CUDA;
+  }
+
+  Params p;
+  p.T = T;
+  p.G = q.G;
+  p.N = q.N;
+  p.K = q.K;
+  p.m_tiles = static_cast<int>((T + kBM - 1) / kBM);
+  p.n_tiles = q.N / kBN;
+  p.num_tiles = p.m_tiles * p.n_tiles * q.G;
+  p.k_blocks = q.K / kBK;
+  p.t_al = t_al;
+  p.b_scale = q.b_scale;
+  p.b_scale_ld = q.K / 128;
+  p.out = static_cast<__nv_bfloat16*>(q.out_bf16);
+  p.q_out = q.q_out;
+  p.q_scale = q.q_scale;
+  p.status = dev.status;
+
+  const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
+  block_scaled_gemm_kernel<kEpi><<<grid, kThreads, kSmemBytes, stream>>>(tm_a, tm_b, tm_sfa, p);
+  return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_block_scaled_gemm(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
+  if (q.K / 128 > 4 * 32 * 4) return DSV4_ERR_UNSUPPORTED;  // weight-scale words held per lane
+  if (q.epilogue == kEpiQuant) return launch_impl<kEpiQuant>(q, stream, dev);
+  return launch_impl<kEpiBf16>(q, stream, dev);
+}
+
+}  // namespace dsv4

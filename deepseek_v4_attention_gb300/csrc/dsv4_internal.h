@@ -1,0 +1,49 @@
+// dsv4_internal.h -- declarations shared by the library's translation units
+// (host side only; no device code here).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dsv4 {
+
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  int cc_major = 0;
+  int cc_minor = 0;
+  size_t max_smem_optin = 0;
+  int* status = nullptr;  // device address of the status word on this device
+};
+
+// Epilogue of the block-scaled GEMM.
+enum GemmEpilogue : int {
+  kEpiBf16 = 0,   // store fp32 accumulators as bf16 rows [T][G*N]
+  kEpiQuant = 1,  // round to bf16, then per-128 UE8M0 FP8 re-quantisation of each row
+};
+
+struct GemmProblem {
+  int64_t T = 0;          // rows (tokens)
+  int G = 1;              // groups: group g of A meets rows g*N:(g+1)*N of B
+  int N = 0;              // output columns per group (multiple of 128)
+  int K = 0;              // reduction length (multiple of 128)
+  const void* a = nullptr;          // e4m3 physical [G][T][K]
+  const int32_t* a_scale = nullptr; // int32 physical [G][ceil(K/512)][T_al]
+  const void* b = nullptr;          // e4m3 [G*N][K] row-major
+  const uint8_t* b_scale = nullptr; // UE8M0 bytes [G*N/128][K/128]
+  int epilogue = kEpiBf16;
+  void* out_bf16 = nullptr;         // bf16 [T][G*N] (required for kEpiBf16, optional for kEpiQuant)
+  uint8_t* q_out = nullptr;         // e4m3 [T][G*N]           (kEpiQuant)
+  int32_t* q_scale = nullptr;       // int32 [ceil(G*N/512)][T_al] (kEpiQuant)
+};
+
+int get_device_info(DeviceInfo* out);
+
+int launch_inv_rope_fp8_quant(const void* o, const int64_t* positions, const float* cache,
+                              int64_t T, int64_t max_pos, int n_groups, int hpg, void* out_fp8,
+                              int32_t* out_scale, cudaStream_t stream, const DeviceInfo& dev);
+
+int launch_block_scaled_gemm(const GemmProblem& p, cudaStream_t stream, const DeviceInfo& dev);
+
+}  // namespace dsv4

@@ -1,0 +1,187 @@
+// dsv4_quant.cu -- fused inverse RoPE + block-scaled FP8 quantisation
+// (vLLM docs, models/deepseek_v4/common/ops/fused_inv_rope_fp8_quant, with the
+// SM100-family packed UE8M0 scale layout).
+//
+// Work unit: one (token t, head h) pair = 512 bf16 = 1 KiB in, 512 B of e4m3
+// + one packed int32 out.  One warp per unit; lane l holds elements
+// [8l, 8l+8) and [256+8l, 256+8l+8) as two 16-byte loads, so each load
+// instruction of the warp reads 512 contiguous bytes.
+//   - 128-element blocks: lanes 0-15 / 16-31 of the first vector are blocks
+//     0 / 1 of the head, of the second vector blocks 2 / 3; a block's amax is
+//     a 4-step xor-shuffle inside one half-warp.
+//   - the 64 rope lanes (head offsets 448..511) are lanes 24-31 of the second
+//     vector; an interleaved pair (2i, 2i+1) never straddles a 16-byte vector,
+//     so the rotation needs no shuffle.  Those lanes read cos[4(l-24)..+3] and
+//     sin[4(l-24)..+3] of row positions[t] as two float4 loads.
+//   - rotation in fp32 with a fixed order: y0 = fma(a, c, b*s),
+//     y1 = fma(b, c, -(a*s)), each cross product rounded first.
+//   - exponent from the fp32 bits of the amax (no log, no division);
+//     q = y * 2^-e is exact; cvt.rn.satfinite to e4m3.
+// Units are walked by a grid-stride loop in (t, h) order, so consecutive warps
+// stream consecutive KiB of o; kUnroll units are loaded before any is
+// processed to keep enough bytes in flight.
+#include "dsv4_device.cuh"
+#include "dsv4_internal.h"
+
+namespace dsv4 {
+
+namespace {
+
+constexpr int kHeadDim = 512;
+constexpr int kRope = 64;
+constexpr int kUnroll = 2;
+
+struct Unit {
+  uint4 v0, v1;     // 8 bf16 each
+  float4 c, s;      // cos / sin of this lane's 4 pairs (lanes 24-31 only)
+  bool valid;
+  bool rotate;
+  int64_t t;
+  int h;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ void inv_rotate(float& a, float& b, float c, float s) {
+  const float bs = __fmul_rn(b, s);
+  const float as = __fmul_rn(a, s);
+  const float y0 = __fmaf_rn(a, c, bs);
+  const float y1 = __fmaf_rn(b, c, -as);
+  a = y0;
+  b = y1;
+}
+
+__device__ __forceinline__ float half_warp_max(float v) {
+#pragma unroll
+  for (int m = 8; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+  return v;
+}
+
+// Quantises 8 values with scale 2^e into 8 e4m3 bytes.
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float inv_scale) {
+  uint2 r;
+  r.x = static_cast<uint32_t>(e4m3x2(f[0] * inv_scale, f[1] * inv_scale)) |
+        (static_cast<uint32_t>(e4m3x2(f[2] * inv_scale, f[3] * inv_scale)) << 16);
+  r.y = static_cast<uint32_t>(e4m3x2(f[4] * inv_scale, f[5] * inv_scale)) |
+        (static_cast<uint32_t>(e4m3x2(f[6] * inv_scale, f[7] * inv_scale)) << 16);
+  return r;
+}
+
+__global__ void __launch_bounds__(256) inv_rope_fp8_quant_kernel(
+    const uint16_t* __restrict__ o, const int64_t* __restrict__ positions,
+    const float* __restrict__ cache, int64_t T, int64_t max_pos, int H, int hpg,
+    uint8_t* __restrict__ out_fp8, int32_t* __restrict__ out_scale, int64_t T_al,
+    int* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t units = T * H;
+  const int64_t D = static_cast<int64_t>(hpg) * kHeadDim;
+  const bool rope_lane = lane >= 24;
+  const int pair0 = 4 * (lane - 24);  // first rope pair of this lane (lanes 24-31)
+
+  for (int64_t base = warp * kUnroll; base < units; base += nwarps * kUnroll) {
+    Unit u[kUnroll];
+    // ---- issue every load of kUnroll units first
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+      const int64_t id = base + k;
+      u[k].valid = id < units;
+      u[k].t = u[k].valid ? id / H : 0;
+      u[k].h = u[k].valid ? static_cast<int>(id - u[k].t * H) : 0;
+      u[k].rotate = false;
+      if (u[k].valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(o + (u[k].t * H + u[k].h) * kHeadDim);
+        u[k].v0 = __ldcs(src + lane);
+        u[k].v1 = __ldcs(src + 32 + lane);
+        if (rope_lane) {
+          const int64_t p = __ldg(positions + u[k].t);
+          if (p >= 0 && p < max_pos) {
+            const float4* row = reinterpret_cast<const float4*>(cache + p * kRope);
+            u[k].c = __ldg(row + (pair0 >> 2));
+            u[k].s = __ldg(row + 8 + (pair0 >> 2));
+            u[k].rotate = true;
+          } else {
+            record_status(status, DSV4_ERR_RANGE);
+          }
+        }
+      }
+    }
+    // ---- rotate, reduce, quantise, store
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+      if (!u[k].valid) continue;  // warp-uniform
+      float f0[8], f1[8];
+      unpack8(u[k].v0, f0);
+      unpack8(u[k].v1, f1);
+      if (u[k].rotate) {
+        inv_rotate(f1[0], f1[1], u[k].c.x, u[k].s.x);
+        inv_rotate(f1[2], f1[3], u[k].c.y, u[k].s.y);
+        inv_rotate(f1[4], f1[5], u[k].c.z, u[k].s.z);
+        inv_rotate(f1[6], f1[7], u[k].c.w, u[k].s.w);
+      }
+      float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        m0 = fmaxf(m0, fabsf(f0[j]));
+        m1 = fmaxf(m1, fabsf(f1[j]));
+      }
+      m0 = half_warp_max(m0);
+      m1 = half_warp_max(m1);
+      const int e0 = ue8m0_exponent(m0);
+      const int e1 = ue8m0_exponent(m1);
+      const uint2 q0 = quant8(f0, exp2_neg(e0));
+      const uint2 q1 = quant8(f1, exp2_neg(e1));
+
+      const int g = u[k].h / hpg;
+      const int hh = u[k].h - g * hpg;
+      uint8_t* dst = out_fp8 + (static_cast<int64_t>(g) * T + u[k].t) * D +
+                     static_cast<int64_t>(hh) * kHeadDim;
+      __stcs(reinterpret_cast<uint2*>(dst) + lane, q0);
+      __stcs(reinterpret_cast<uint2*>(dst + 256) + lane, q1);
+
+      // bytes: block 0 = e0 of lanes 0-15, block 1 = e0 of lanes 16-31,
+      //        block 2 = e1 of lanes 0-15, block 3 = e1 of lanes 16-31
+      const uint32_t b0 = static_cast<uint32_t>(e0 + 127);
+      const uint32_t b2 = static_cast<uint32_t>(e1 + 127);
+      const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, b0, 16);
+      const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, b2, 16);
+      if (lane == 0) {
+        const uint32_t word = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        out_scale[(static_cast<int64_t>(g) * hpg + hh) * T_al + u[k].t] =
+            static_cast<int32_t>(word);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+int launch_inv_rope_fp8_quant(const void* o, const int64_t* positions, const float* cache,
+                              int64_t T, int64_t max_pos, int n_groups, int hpg,
+                              void* out_fp8, int32_t* out_scale, cudaStream_t stream,
+                              const DeviceInfo& dev) {
+  const int H = n_groups * hpg;
+  const int64_t units = T * H;
+  const int64_t T_al = (T + 3) / 4 * 4;
+  const int threads = 256;
+  const int64_t warps_needed = (units + kUnroll - 1) / kUnroll;
+  int64_t blocks = (warps_needed * 32 + threads - 1) / threads;
+  const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * (2048 / threads);
+  if (blocks > max_blocks) blocks = max_blocks;
+  if (blocks < 1) blocks = 1;
+  inv_rope_fp8_quant_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      static_cast<const uint16_t*>(o), positions, cache, T, max_pos, H, hpg,
+      static_cast<uint8_t*>(out_fp8), out_scale, T_al, dev.status);
+  return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+}  // namespace dsv4

@@ -1,0 +1,172 @@
+/*
+ * dsv4.h -- C ABI of the DeepSeek-V4 attention O-projection hot path on
+ * GB300 (sm_103a).
+ *
+ * The path (vLLM docs, models/deepseek_v4/nvidia/ops/o_proj,
+ * deep_gemm_fp8_o_proj):
+ *     o --(inverse RoPE + per-128 FP8 quant)--> x, sx
+ *       --(grouped wo_a, group g meets rows g*R:(g+1)*R)--> z [T, G, R] bf16
+ *       --(wo_b over z.flatten(1))--> out [T, hidden] bf16
+ *
+ * Conventions for every entry point:
+ *   - Sizes are int64_t or int.  Pointers marked "device" must be device
+ *     memory of the current CUDA device (or managed memory); the caller owns
+ *     every buffer.  The library never allocates, frees or synchronises in a
+ *     compute call: it validates, then enqueues kernels on `stream` (a
+ *     cudaStream_t; NULL is the legacy default stream) and returns.
+ *   - Every argument is checked on the host before any launch.  On a host
+ *     error nothing is written and a negative dsv4_status is returned.  T == 0
+ *     is valid and launches nothing.
+ *   - Data-dependent faults (an out-of-range position, a pipeline wait that
+ *     exceeded its limit) cannot be seen before the launch: the kernels record
+ *     them in a device status word and never trap.  Read it with
+ *     dsv4_device_status().
+ *   - Inputs must be finite (the pages say nothing about NaN/Inf handling).
+ *   - Calls on the same stream are ordered; concurrent calls on different
+ *     streams that share output buffers race, as for any kernel.
+ */
+#ifndef DSV4_H
+#define DSV4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dsv4_status {
+    DSV4_OK = 0,
+    DSV4_ERR_SHAPE = -1,       /* a shape assert of fused_inv_rope_fp8_quant, or a size rule below */
+    DSV4_ERR_NULL = -2,        /* a required pointer is NULL                                      */
+    DSV4_ERR_ALIGN = -3,       /* a base pointer is not 16-byte aligned (TMA and vector loads)    */
+    DSV4_ERR_UNSUPPORTED = -4, /* not an sm_103 device, or a parameter this build does not serve  */
+    DSV4_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than dsv4_o_proj_workspace_bytes()    */
+    DSV4_ERR_CUDA = -6,        /* a CUDA runtime/driver call failed (launch error included)       */
+    DSV4_ERR_TIMEOUT = -7,     /* device status: a kernel pipeline wait ran out of time           */
+    DSV4_ERR_RANGE = -8        /* device status: a position outside [0, max_pos)                  */
+} dsv4_status;
+
+/*
+ * Fused inverse RoPE + block-scaled FP8 quantisation.
+ *
+ * Follows vLLM docs, models/deepseek_v4/common/ops/fused_inv_rope_fp8_quant
+ * (signature, parameter table, shape asserts, derived sizes), with
+ * tma_aligned_scales=True: the SM100-family layout that
+ * compute_fp8_einsum_recipe picks for cap.major >= 10 (o_proj page), which
+ * includes GB300.  The rotated lanes are the last rope_dim of each head
+ * (sglang deepseek_v4.py, MQALayer.forward: o[..., -qk_rope_head_dim:] with
+ * inverse=True), paired GPT-J style (rotary_emb built with
+ * is_neox_style=False): (a, b) = (x[nope+2i], x[nope+2i+1]) becomes
+ * (a c + b s, b c - a s) with c = cache[p][i], s = cache[p][rope/2 + i].
+ *
+ *   o              device bf16 [T, H, head_dim] contiguous, H = n_groups*heads_per_group
+ *   positions      device int64 [T], each in [0, max_pos)
+ *   cos_sin_cache  device fp32 [max_pos, rope_dim] contiguous: cos || sin
+ *   out_fp8        device e4m3 bytes, physical [G][T][D], D = heads_per_group*head_dim:
+ *                  the page's [T, G, D] view with strides (D, T*D, 1)
+ *   out_scale      device int32, physical [G][PK][T_al], PK = ceil(D/qgs/4),
+ *                  T_al = T rounded up to a multiple of 4 (get_tma_aligned_size(T, 4)):
+ *                  the page's [T, G, PK] view with strides (1, PK*T_al, T_al).
+ *                  Block kb of row (t, g) is byte kb % 4 (little-endian) of
+ *                  int32 kb / 4; the byte is e + 127 for the scale 2^e, e the
+ *                  smallest integer with max(amax, 1e-4) <= 448 * 2^e.  Pad
+ *                  columns [T, T_al) are not written.
+ *
+ * Errors: DSV4_ERR_SHAPE for a failed page assert (H != G*hpg, head_dim !=
+ * nope+rope, head_dim % qgs, nope % qgs != qgs - rope, odd rope, T < 0,
+ * max_pos <= 0); DSV4_ERR_UNSUPPORTED unless nope_dim = 448, rope_dim = 64,
+ * quant_group_size = 128 (the only configuration the pages use);
+ * DSV4_ERR_NULL / DSV4_ERR_ALIGN for pointers (all 16-byte aligned).
+ * A position outside [0, max_pos) sets DSV4_ERR_RANGE in the device status
+ * word; that token's rope lanes are then quantised unrotated.
+ */
+int dsv4_inv_rope_fp8_quant(const void* o, const int64_t* positions, const float* cos_sin_cache,
+                            int64_t num_tokens, int64_t max_pos, int n_groups,
+                            int heads_per_group, int nope_dim, int rope_dim,
+                            int quant_group_size, void* out_fp8, int32_t* out_scale,
+                            void* stream);
+
+/*
+ * Grouped wo_a projection with block-scaled FP8 operands.
+ *
+ * Follows vLLM docs, models/deepseek_v4/common/grouped_wo_a (group g of the
+ * inverse-rotated output meets only rows g*R:(g+1)*R) and o_proj page,
+ * deep_gemm_fp8_o_proj: fp8_einsum("bhr,hdr->bhd") with recipe (1, 1, 128)
+ * into a bf16 z [T, G, R]; weight scales are 128 x 128 blocks (sglang
+ * deepseek_v4.py, _dequant_fp8).
+ *     z[t, g, n] = bf16( sum_k x[t,g,k] 2^ex[t,g,k/128] * W[g*R+n,k] 2^ew[(g*R+n)/128, k/128] )
+ * accumulated in fp32 on the tensor cores.
+ *
+ *   x_fp8    device e4m3 physical [G][T][D]   (out_fp8 of the call above)
+ *   x_scale  device int32 physical [G][PK][T_al] (out_scale of the call above)
+ *   w_fp8    device e4m3 [G*R, D] row-major (wo_a.weight)
+ *   w_scale  device UE8M0 raw bytes [G*R/128, D/128] row-major
+ *   z        device bf16 [T, G, R] contiguous
+ *
+ * Errors: DSV4_ERR_SHAPE unless D and R are positive multiples of 128 and
+ * T >= 0; DSV4_ERR_NULL / DSV4_ERR_ALIGN (16 bytes) for pointers.
+ */
+int dsv4_grouped_wo_a(const void* x_fp8, const int32_t* x_scale, int64_t num_tokens,
+                      int n_groups, int group_dim, int o_lora_rank, const void* w_fp8,
+                      const uint8_t* w_scale, void* z, void* stream);
+
+/*
+ * Bytes of caller-owned scratch that dsv4_o_proj needs for these sizes: the
+ * quantised groups x [G][T][D] with their scales [G][PK][T_al], and the
+ * per-128 re-quantised z [T][G*R] with its scales [G*R/512][T_al] (each part
+ * 256-byte aligned).  Returns 0 for invalid sizes.
+ */
+size_t dsv4_o_proj_workspace_bytes(int64_t num_tokens, int n_groups, int heads_per_group,
+                                   int head_dim, int o_lora_rank);
+
+/*
+ * The whole O-projection (o_proj page, deep_gemm_fp8_o_proj with an FP8
+ * wo_b): inverse RoPE + FP8 quant of o, the grouped wo_a GEMM, the per-128
+ * UE8M0 re-quantisation of the bf16 z.flatten(1) (fused into the wo_a
+ * epilogue: z is rounded to bf16 first, then quantised exactly as a stored z
+ * would be), and the dense wo_b GEMM
+ *     out[t, h] = bf16( sum_c zq[t,c] 2^ez[t,c/128] * Wb[h,c] 2^eb[h/128, c/128] ).
+ * The activation quantisation inside wo_b is not printed on the pages; this
+ * is its plainest reading (the same per-128 UE8M0 rule as wo_a's input).
+ *
+ *   o, positions, cos_sin_cache, max_pos, sizes: as dsv4_inv_rope_fp8_quant
+ *   wo_a_fp8, wo_a_scale : as dsv4_grouped_wo_a (w_fp8, w_scale)
+ *   wo_b_fp8             device e4m3 [hidden, G*R] row-major
+ *   wo_b_scale           device UE8M0 raw bytes [hidden/128, G*R/128]
+ *   out                  device bf16 [T, hidden] contiguous
+ *   workspace            device scratch of at least dsv4_o_proj_workspace_bytes()
+ *                        bytes, 256-byte aligned; its contents are clobbered.
+ *
+ * Errors: as the two calls above, plus DSV4_ERR_SHAPE unless hidden is a
+ * positive multiple of 128, DSV4_ERR_WORKSPACE if the workspace is NULL or too
+ * small, DSV4_ERR_ALIGN if it is not 256-byte aligned.
+ */
+int dsv4_o_proj(const void* o, const int64_t* positions, const float* cos_sin_cache,
+                int64_t max_pos, int64_t num_tokens, int n_groups, int heads_per_group,
+                int nope_dim, int rope_dim, int quant_group_size, int o_lora_rank, int hidden,
+                const void* wo_a_fp8, const uint8_t* wo_a_scale, const void* wo_b_fp8,
+                const uint8_t* wo_b_scale, void* out, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/* Human-readable name of a dsv4_status value (static string). */
+const char* dsv4_status_string(int status);
+
+/*
+ * Reads the device status word of the current device (the first data-dependent
+ * error any kernel recorded since the last clear: DSV4_ERR_RANGE or
+ * DSV4_ERR_TIMEOUT, else DSV4_OK).  Synchronises `stream` first.  If `clear`
+ * is non-zero the word is reset to DSV4_OK.  Returns DSV4_ERR_CUDA if the
+ * read itself fails.
+ */
+int dsv4_device_status(void* stream, int clear);
+
+/* Number of kernel launches the last successful compute call on this host
+ * thread enqueued (0 for T == 0).  For accounting in benchmarks. */
+int dsv4_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSV4_H */

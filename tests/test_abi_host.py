@@ -1,0 +1,102 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports every
+function include/dsv4.h declares, and its host-side validation rejects bad
+arguments before touching CUDA.  No compute call is made here."""
+import ctypes
+import subprocess
+
+import pytest
+
+import deepseek_v4_attention_gb300 as k
+from deepseek_v4_attention_gb300 import _build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return k.load_library()
+
+
+def test_exports_every_header_function(lib):
+    names = k.header_functions()
+    assert set(names) == {"dsv4_inv_rope_fp8_quant", "dsv4_grouped_wo_a",
+                          "dsv4_o_proj_workspace_bytes", "dsv4_o_proj", "dsv4_status_string",
+                          "dsv4_device_status", "dsv4_last_launch_count"}
+    out = subprocess.run(["nm", "-D", "--defined-only", k.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for code, name in k.STATUS.items():
+        assert k.dsv4_status_string(code).startswith(name)
+    assert "unknown" in k.dsv4_status_string(12345)
+
+
+def test_quant_host_validation_without_gpu(lib):
+    f = lib.dsv4_inv_rope_fp8_quant
+    P = 4096  # any non-null, 16-byte aligned fake address: rejected before use
+    good = [P, P, P, 4, 16, 2, 2, 448, 64, 128, P, P, None]
+    for idx, val, rc in [(3, -1, -1), (4, 0, -1), (5, 0, -1), (6, 0, -1), (8, 63, -1),
+                         (9, 100, -1), (9, 32, -1), (7, 192, -4), (9, 0, -1)]:
+        a = list(good); a[idx] = val
+        assert f(*a) == rc, (idx, val)
+    # T == 0 is valid and launches nothing, even with null pointers
+    a = list(good); a[3] = 0; a[0] = None
+    assert f(*a) == 0 and k.dsv4_last_launch_count() == 0
+    for idx in (0, 1, 2, 10, 11):
+        a = list(good); a[idx] = None
+        assert f(*a) == -2
+    for idx in (0, 1, 2, 10, 11):
+        a = list(good); a[idx] = P + 4
+        assert f(*a) == -3
+
+
+def test_gemm_host_validation_without_gpu(lib):
+    f = lib.dsv4_grouped_wo_a
+    P = 4096
+    good = [P, P, 16, 2, 1024, 128, P, P, P, None]
+    for idx, val in [(2, -1), (3, 0), (4, 1000), (5, 100), (4, 0), (5, 0)]:
+        a = list(good); a[idx] = val
+        assert f(*a) == -1, (idx, val)
+    a = list(good); a[2] = 0
+    assert f(*a) == 0
+    for idx in (0, 1, 6, 7, 8):
+        a = list(good); a[idx] = None
+        assert f(*a) == -2
+    for idx in (0, 1, 6, 8):
+        a = list(good); a[idx] = P + 8
+        assert f(*a) == -3
+
+
+def test_o_proj_workspace_bytes(lib):
+    T, G, hpg, R = 4096, 16, 8, 1024
+    need = k.dsv4_o_proj_workspace_bytes(T, G, hpg, 512, R)
+    D = hpg * 512
+    expect = G * T * D + G * (D // 512) * T * 4 + T * G * R + (G * R // 512) * T * 4
+    assert need == expect                  # every part is already a multiple of 256 here
+    assert k.dsv4_o_proj_workspace_bytes(5, 2, 2, 512, 128) % 256 == 0
+    assert k.dsv4_o_proj_workspace_bytes(-1, 2, 2, 512, 128) == 0
+    assert k.dsv4_o_proj_workspace_bytes(4, 2, 2, 500, 128) == 0
+
+
+def test_o_proj_host_validation_without_gpu(lib):
+    f = lib.dsv4_o_proj
+    P = 4096
+    need = k.dsv4_o_proj_workspace_bytes(16, 2, 2, 512, 128)
+    good = [P, P, P, 4096, 16, 2, 2, 448, 64, 128, 128, 256, P, P, P, P, P, 1 << 20, need, None]
+    for idx, val, rc in [(4, -1, -1), (10, 100, -1), (11, 100, -1), (11, 0, -1), (3, 0, -1),
+                         (9, 64, -4), (7, 192, -4), (9, 32, -1)]:
+        a = list(good); a[idx] = val
+        assert f(*a) == rc, (idx, val)
+    a = list(good); a[18] = need - 1
+    assert f(*a) == -5
+    a = list(good); a[17] = None
+    assert f(*a) == -5
+    a = list(good); a[17] = (1 << 20) + 16
+    assert f(*a) == -3
+    for idx in (0, 1, 2, 12, 13, 14, 15, 16):
+        a = list(good); a[idx] = None
+        assert f(*a) == -2, idx

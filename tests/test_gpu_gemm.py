@@ -1,0 +1,181 @@
+"""GPU parity of dsv4_grouped_wo_a and dsv4_o_proj against the CPU oracle
+(through the C ABI).  Tolerance: gpu_helpers.GEMM_RTOL."""
+import numpy as np
+import pytest
+import torch
+
+import dsv4_inputs as di
+import oracle
+from gpu_helpers import GEMM_RTOL, assert_codes_match, cuda_or_skip, gemm_rel_err, to_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return cuda_or_skip()
+
+
+def _gpu_wo_a(x, xs, w, ws, T, G, D, R, dev):
+    import deepseek_v4_attention_gb300 as k
+    xg = x.to(dev).view(torch.float8_e4m3fn)            # physical [G, T, D]
+    sg = xs.to(dev)                                     # physical [G, PK, T_al]
+    z = k.dsv4_grouped_wo_a(xg.transpose(0, 1), sg.permute(2, 0, 1)[:T], w.to(dev),
+                            ws.to(dev), G, R)
+    torch.cuda.synchronize()
+    assert k.dsv4_device_status(clear=True) == 0
+    return to_bits(z)
+
+
+@pytest.mark.parametrize("T,G,D,R", [(16, 2, 1024, 128), (64, 8, 4096, 1024), (1, 1, 128, 128),
+                                     (3, 2, 512, 256), (129, 3, 640, 384), (200, 1, 1024, 896)])
+def test_grouped_wo_a_random_operands(dev, T, G, D, R):
+    T_al = oracle.tma_aligned_tokens(T)
+    x, xs = di.random_fp8_activation(T, G, D, seed=T * 7 + G, tma_aligned_T=T_al)
+    w, ws = di.fp8_block_weight(G * R, D, seed=T + 1000 * G)
+    zg = _gpu_wo_a(x, xs, w, ws, T, G, D, R, dev)
+    zr, z64 = oracle.grouped_gemm(x, xs, w, ws, T, G, D, R, want_fp64=True)
+    err = gemm_rel_err(zg, z64)
+    assert err <= GEMM_RTOL, err
+
+
+def test_grouped_wo_a_identity_weight_is_exact(dev):
+    """W = I in every group with unit scales: z must equal bf16(dq_x) exactly."""
+    T, G, D, R = 130, 2, 512, 256
+    T_al = oracle.tma_aligned_tokens(T)
+    x, xs = di.random_fp8_activation(T, G, D, seed=5, tma_aligned_T=T_al)
+    w = torch.zeros(G * R, D, dtype=torch.uint8)
+    for g in range(G):
+        w[g * R:(g + 1) * R, :R] = torch.eye(R, dtype=torch.uint8) * 0x38
+    ws = torch.full((G * R // 128, D // 128), 127, dtype=torch.uint8)
+    zg = _gpu_wo_a(x, xs, w, ws, T, G, D, R, dev)
+    zr = oracle.grouped_gemm(x, xs, w, ws, T, G, D, R)
+    assert np.array_equal(zg, zr)
+
+
+def test_grouped_wo_a_scale_rows(dev):
+    """Scales that vary only by token row, and only by k-block: catches a wrong
+    scale-factor layout in tensor memory (exact products, exact sums)."""
+    T, G, D, R = 128, 1, 1024, 128
+    T_al = T
+    codes = torch.full((G, T, D), 0x38, dtype=torch.uint8)          # all ones
+    b = torch.zeros((G, 8, T_al), dtype=torch.int64)
+    row_e = torch.arange(T) % 7                                      # per-row exponent
+    for kb in range(8):
+        b[:, kb, :] = 120 + row_e + kb                              # + per-block exponent
+    words = (b[:, 0::4] | (b[:, 1::4] << 8) | (b[:, 2::4] << 16) | (b[:, 3::4] << 24))
+    words = torch.where(words >= 2 ** 31, words - 2 ** 32, words).to(torch.int32)
+    w = torch.full((R, D), 0x38, dtype=torch.uint8)
+    ws = torch.full((1, 8), 127, dtype=torch.uint8)
+    ws[0, 3] = 125
+    zg = _gpu_wo_a(codes, words, w, ws, T, G, D, R, dev)
+    zr = oracle.grouped_gemm(codes, words, w, ws, T, G, D, R)
+    assert np.array_equal(zg, zr)
+
+
+def test_grouped_wo_a_decode_config_parity(dev):
+    w = di.WORKLOADS["decode"]
+    d = di.make_inputs(w, with_wo_b=False)
+    x, xs = oracle.inv_rope_fp8_quant(d["o"], d["positions"], d["cache"], w.n_groups,
+                                      w.heads_per_group)
+    x, xs = torch.from_numpy(x), torch.from_numpy(xs)
+    zg = _gpu_wo_a(x, xs, d["wo_a"], d["wo_a_scale"], w.T, w.n_groups, w.D, w.o_lora_rank, dev)
+    _, z64 = oracle.grouped_gemm(x, xs, d["wo_a"], d["wo_a_scale"], w.T, w.n_groups, w.D,
+                                 w.o_lora_rank, want_fp64=True)
+    assert gemm_rel_err(zg, z64) <= GEMM_RTOL
+
+
+def test_grouped_wo_a_prefill_config_sampled(dev):
+    """T = 8192 prefill workload (all groups, all columns) checked on a seeded
+    sample of 256 token rows (the product is row-independent)."""
+    import deepseek_v4_attention_gb300 as k
+    w = di.WORKLOADS["prefill"]
+    d = di.make_inputs(w, with_wo_b=False)
+    q, s = k.dsv4_inv_rope_fp8_quant(d["o"].to(dev), d["positions"].to(dev), d["cache"].to(dev),
+                                     w.n_groups, w.heads_per_group)
+    z = k.dsv4_grouped_wo_a(q, s, d["wo_a"].to(dev), d["wo_a_scale"].to(dev), w.n_groups,
+                            w.o_lora_rank)
+    torch.cuda.synchronize()
+    assert k.dsv4_device_status(clear=True) == 0
+    idx = np.sort(np.random.default_rng(0).choice(w.T, 256, replace=False))
+    ti = torch.from_numpy(idx)
+    xr, xsr = oracle.inv_rope_fp8_quant(d["o"][ti], d["positions"][ti], d["cache"], w.n_groups,
+                                        w.heads_per_group)
+    # the GPU's own quantised rows are what its GEMM consumed; they match the oracle's
+    qg = to_bits(q.view(torch.uint8).transpose(0, 1))[:, idx]
+    assert_codes_match(qg, xr)
+    _, z64 = oracle.grouped_gemm(xr, xsr, d["wo_a"], d["wo_a_scale"], len(idx), w.n_groups, w.D,
+                                 w.o_lora_rank, want_fp64=True)
+    zg = to_bits(z)[idx]
+    assert gemm_rel_err(zg, z64) <= GEMM_RTOL
+
+
+def _o_proj_gpu(d, w, dev, T=None):
+    import deepseek_v4_attention_gb300 as k
+    out = k.dsv4_o_proj(d["o"].to(dev), d["positions"].to(dev), d["cache"].to(dev),
+                        d["wo_a"].to(dev), d["wo_a_scale"].to(dev), d["wo_b"].to(dev),
+                        d["wo_b_scale"].to(dev), n_groups=w.n_groups,
+                        heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank)
+    assert k.dsv4_last_launch_count() == 3
+    torch.cuda.synchronize()
+    assert k.dsv4_device_status(clear=True) == 0
+    return to_bits(out)
+
+
+@pytest.mark.parametrize("T", [16, 1, 5, 131])
+def test_o_proj_tiny_parity(dev, T):
+    w = di.WORKLOADS["tiny"].with_tokens(T, seed=T)
+    d = di.make_inputs(w)
+    og = _o_proj_gpu(d, w, dev)
+    _, out64, _ = oracle.o_proj(d["o"], d["positions"], d["cache"], d["wo_a"], d["wo_a_scale"],
+                                d["wo_b"], d["wo_b_scale"], n_groups=w.n_groups,
+                                heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank,
+                                hidden=w.hidden)
+    assert gemm_rel_err(og, out64) <= GEMM_RTOL
+
+
+def test_o_proj_full_config_sampled(dev):
+    """Full workload (T=4096, 128 heads, R=1024, hidden 7168) in the launch
+    configuration the benchmark times; 24 seeded token rows checked against the
+    oracle's whole chain (the path is row-independent)."""
+    w = di.WORKLOADS["full"]
+    d = di.make_inputs(w)
+    og = _o_proj_gpu(d, w, dev)
+    idx = np.sort(np.random.default_rng(1).choice(w.T, 24, replace=False))
+    ti = torch.from_numpy(idx)
+    _, out64, _ = oracle.o_proj(d["o"][ti], d["positions"][ti], d["cache"], d["wo_a"],
+                                d["wo_a_scale"], d["wo_b"], d["wo_b_scale"], n_groups=w.n_groups,
+                                heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank,
+                                hidden=w.hidden)
+    assert gemm_rel_err(og[idx], out64) <= GEMM_RTOL
+    og2 = _o_proj_gpu(d, w, dev)
+    assert np.array_equal(og, og2), "two runs differ"
+
+
+def test_o_proj_errors(dev):
+    import deepseek_v4_attention_gb300 as k
+    lib = k.load_library()
+    w = di.WORKLOADS["tiny"]
+    d = {n: t.to(dev) for n, t in di.make_inputs(w).items()}
+    out = torch.empty(w.T, w.hidden, dtype=torch.bfloat16, device=dev)
+    need = k.dsv4_o_proj_workspace_bytes(w.T, w.n_groups, w.heads_per_group, 512, w.o_lora_rank)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    args = [d["o"].data_ptr(), d["positions"].data_ptr(), d["cache"].data_ptr(), w.max_pos, w.T,
+            w.n_groups, w.heads_per_group, 448, 64, 128, w.o_lora_rank, w.hidden,
+            d["wo_a"].data_ptr(), d["wo_a_scale"].data_ptr(), d["wo_b"].data_ptr(),
+            d["wo_b_scale"].data_ptr(), out.data_ptr(), ws.data_ptr(), need, None]
+    assert lib.dsv4_o_proj(*args) == 0
+    bad = list(args); bad[18] = need - 1
+    assert lib.dsv4_o_proj(*bad) == -5
+    bad = list(args); bad[17] = None
+    assert lib.dsv4_o_proj(*bad) == -5
+    bad = list(args); bad[17] = ws.data_ptr() + 16; bad[18] = need + 16
+    assert lib.dsv4_o_proj(*bad) == -3
+    bad = list(args); bad[11] = 200
+    assert lib.dsv4_o_proj(*bad) == -1
+    bad = list(args); bad[10] = 100
+    assert lib.dsv4_o_proj(*bad) == -1
+    bad = list(args); bad[4] = 0
+    assert lib.dsv4_o_proj(*bad) == 0 and k.dsv4_last_launch_count() == 0
+    torch.cuda.synchronize()
+    assert k.dsv4_device_status(clear=True) == 0
