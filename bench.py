@@ -1,0 +1,361 @@
+"""Benchmark of the DeepSeek-V4 attention O-projection on GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+inverse RoPE + FP8 quantisation -> grouped wo_a GEMM (with the fused per-128
+re-quantisation of z) -> wo_b GEMM, through the C ABI (dsv4_o_proj).
+Default workload: T = 4096 tokens, 128 heads of 512 (16 groups x 8),
+o_lora_rank 1024, hidden 7168.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  Under torchrun each rank runs its own T tokens
+(weak scaling, replicated weights, no collective on the data path); the
+timing is the max over ranks.  --impl reference times the CPU oracle on a
+bounded token sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import dsv4_inputs as di  # noqa: E402
+
+METRIC = "O-proj tokens/s"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--tokens", type=int, default=None, help="tokens per GPU (default 4096)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload(args) -> di.Workload:
+    w = di.WORKLOADS["full"]
+    if args.tokens:
+        w = w.with_tokens(args.tokens)
+    return w
+
+
+def config_of(w: di.Workload, n_gpus: int) -> dict:
+    return {
+        "workload": f"full O-projection: T={w.T} tokens/GPU, {w.H} heads x 512 "
+                    f"({w.n_groups} groups x {w.heads_per_group}), o_lora_rank {w.o_lora_rank}, "
+                    f"hidden {w.hidden}, positions U[0,{w.max_pos})",
+        "tokens_per_gpu": w.T, "n_groups": w.n_groups, "heads_per_group": w.heads_per_group,
+        "head_dim": w.head_dim, "o_lora_rank": w.o_lora_rank, "hidden": w.hidden,
+        "global_tokens": w.T * n_gpus, "parallelism": f"replicas x{n_gpus} (token shards)",
+        "l2": "inputs larger than L2 (o 537 MB + weights 184 MB streamed per step)",
+    }
+
+
+# ---------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------- our arm --
+def run_ours(args, ws, rank, local):
+    import deepseek_v4_attention_gb300 as k
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = workload(args)
+    w = w.with_tokens(w.T, seed=w.seed + 1000 * rank)       # each rank its own tokens
+    host = di.make_inputs(w)
+    d = {n: t.to(dev) for n, t in host.items()}
+    need = k.dsv4_o_proj_workspace_bytes(w.T, w.n_groups, w.heads_per_group, w.head_dim,
+                                         w.o_lora_rank)
+    wsp = torch.empty(need, dtype=torch.uint8, device=dev)
+    out = torch.empty(w.T, w.hidden, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(n_groups=w.n_groups, heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank,
+              out=out, workspace=wsp)
+    args_dev = [d[n] for n in ("o", "positions", "cache", "wo_a", "wo_a_scale", "wo_b",
+                               "wo_b_scale")]
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if ws == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # per-kernel events, recorded by the library between its three launches
+    n_ev = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
+    for e in evs:                      # create the events outside the timed region
+        for ev in e:
+            ev.record(stream)
+    for _ in range(args.warmup):
+        k.dsv4_o_proj(*args_dev, **kw)
+    torch.cuda.synchronize(dev)
+    if k.dsv4_device_status(clear=True) != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    launches = 0
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            k.dsv4_o_proj(*args_dev, **kw, stage_events=evs[i])
+            launches += k.dsv4_last_launch_count()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    ms_total = max_over_ranks(t0.elapsed_time(t1))
+    if k.dsv4_device_status(clear=True) != 0:
+        raise RuntimeError("device status error in the timed region")
+    ms_step = ms_total / args.steps
+    value = w.T * ws * args.steps / (ms_total / 1e3)
+
+    stage_ms = [0.0, 0.0, 0.0]
+    for e in evs:
+        for j in range(3):
+            stage_ms[j] += e[j].elapsed_time(e[j + 1])
+    stage_ms = [x / n_ev for x in stage_ms]
+
+    # --- e2e: host buffers in, host result out, through the same C-ABI call
+    e2e = None
+    if not args.no_e2e:
+        o_h = host["o"].pin_memory()
+        p_h = host["positions"].pin_memory()
+        out_h = torch.empty(w.T, w.hidden, dtype=torch.bfloat16).pin_memory()
+        o_d, p_d = torch.empty_like(d["o"]), torch.empty_like(d["positions"])
+        e2e_steps = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            o_d.copy_(o_h, non_blocking=True)
+            p_d.copy_(p_h, non_blocking=True)
+            k.dsv4_o_proj(o_d, p_d, *args_dev[2:], **kw)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e_ms = max_over_ranks(a0.elapsed_time(a1))
+        e2e = {"value": w.T * ws * e2e_steps / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": o_h.numel() * 2 + p_h.numel() * 8,
+               "d2h_bytes_per_step": out_h.numel() * 2, "steps": e2e_steps}
+
+    # --- roofline of the dominant kernel (the largest stage time)
+    peaks, src = measured_peaks()
+    T, G, R, D, Hd = w.T, w.n_groups, w.o_lora_rank, w.D, w.hidden
+    fl_a = 2.0 * T * G * R * D
+    fl_b = 2.0 * T * Hd * G * R
+    quant_bytes = T * w.H * (1024 + 512 + 4) + T * (8 + 256)
+    fp8_peak = 2.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])  # fp8 = 2 x bf16
+    stages = {
+        "quant": {"ms": stage_ms[0], "bound": "hbm", "algorithmic": quant_bytes,
+                  "achieved": quant_bytes / (stage_ms[0] * 1e-3) / 1e9, "unit": "GB/s",
+                  "peak": peaks["hbm_gbs"]},
+        "wo_a": {"ms": stage_ms[1], "bound": "tensor", "algorithmic": fl_a,
+                 "achieved": fl_a / (stage_ms[1] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                 "peak": fp8_peak},
+        "wo_b": {"ms": stage_ms[2], "bound": "tensor", "algorithmic": fl_b,
+                 "achieved": fl_b / (stage_ms[2] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                 "peak": fp8_peak},
+    }
+    for s in stages.values():
+        s["frac"] = s["achieved"] / s["peak"]
+    dom = max(stages, key=lambda n: stages[n]["ms"])
+    ds = stages[dom]
+    roofline = {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
+                "peak": ds["peak"], "unit": ds["unit"], "frac": ds["frac"],
+                "traffic": None,
+                "peak_source": f"{src}: " + ("fp8 = 2 x bf16_tflops_sustained"
+                                              if ds["bound"] == "tensor" else "hbm_gbs")}
+
+    clocks = clk.summary()
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded; random FP8 block-scaled weights)",
+        "config": config_of(w, ws), "clocks": clocks, "e2e": e2e,
+        "gpu_launches": launches, "roofline": roofline,
+        "stages": {n: {kk: v for kk, v in s.items()} for n, s in stages.items()},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+# ------------------------------------------------------ oracle (CPU) --
+def _oracle_tokens(w: di.Workload, host: dict, idx, oracle):
+    ti = torch.as_tensor(idx)
+    oracle.o_proj(host["o"][ti], host["positions"][ti], host["cache"], host["wo_a"],
+                  host["wo_a_scale"], host["wo_b"], host["wo_b_scale"], n_groups=w.n_groups,
+                  heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank, hidden=w.hidden)
+
+
+def cpu_baseline(w: di.Workload, seconds: float, host: dict | None = None) -> dict:
+    """The oracle as it stands, on a bounded token sample of the same workload."""
+    import oracle
+    host = host or di.make_inputs(w)
+    threads = oracle.num_threads()
+    n = max(1, threads)
+    t = time.perf_counter()
+    _oracle_tokens(w, host, list(range(n)), oracle)
+    per_tok = (time.perf_counter() - t) / n
+    m = max(n, min(w.T, int(seconds / max(per_tok, 1e-9))))
+    m = max(threads, m // threads * threads)
+    t = time.perf_counter()
+    _oracle_tokens(w, host, list(range(m)), oracle)
+    el = time.perf_counter() - t
+    return {"value": m / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{m} of the workload's {w.T} tokens through the whole O-projection "
+                      f"(plain C, fp64 GEMMs), {el:.1f} s"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    import oracle
+    w = workload(args)
+    host = di.make_inputs(w)
+    threads = oracle.num_threads()
+    # size one step so that warmup + steps take ~90 s in all
+    t = time.perf_counter()
+    _oracle_tokens(w, host, list(range(threads)), oracle)
+    per_tok = (time.perf_counter() - t) / threads
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    n = max(1, min(w.T, int(budget / max(per_tok, 1e-9))))
+    rng = list(range(w.T))
+    for i in range(args.warmup):
+        _oracle_tokens(w, host, rng[(i * n) % w.T:][:n] or rng[:n], oracle)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        s0 = (i * n) % w.T
+        _oracle_tokens(w, host, (rng[s0:] + rng[:s0])[:n], oracle)
+    el = time.perf_counter() - t
+    value = n * args.steps / el
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; random FP8 block-scaled weights)",
+        "config": config_of(w, ws),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{n} tokens per step of the workload's {w.T}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, ws, rank)
+    else:
+        res = run_ours(args, ws, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

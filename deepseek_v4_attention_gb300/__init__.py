@@ -60,6 +60,9 @@ def load_library() -> ctypes.CDLL:
     lib.dsv4_o_proj.argtypes = [P, P, P, I64, I64, I, I, I, I, I, I, I, P, P, P, P, P, P,
                                 ctypes.c_size_t, P]
     lib.dsv4_o_proj.restype = I
+    lib.dsv4_o_proj_with_events.argtypes = [P, P, P, I64, I64, I, I, I, I, I, I, I, P, P, P, P,
+                                            P, P, ctypes.c_size_t, P, P]
+    lib.dsv4_o_proj_with_events.restype = I
     lib.dsv4_status_string.argtypes = [I]
     lib.dsv4_status_string.restype = ctypes.c_char_p
     lib.dsv4_device_status.argtypes = [P, I]
@@ -182,8 +185,12 @@ def dsv4_o_proj(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.T
                 wo_b_scale: torch.Tensor, *, n_groups: int, heads_per_group: int,
                 o_lora_rank: int, nope_dim: int = 448, rope_dim: int = 64,
                 quant_group_size: int = 128, out: torch.Tensor | None = None,
-                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """The whole O-projection: returns bf16 out [T, hidden]."""
+                workspace: torch.Tensor | None = None, stage_events=None,
+                stream=None) -> torch.Tensor:
+    """The whole O-projection: returns bf16 out [T, hidden].
+
+    stage_events: optional list of 4 torch.cuda.Event(enable_timing=True),
+    recorded before the first kernel and after each of the three kernels."""
     lib = load_library()
     _cuda(o, "o", torch.bfloat16)
     _cuda(positions, "positions", torch.int64)
@@ -214,11 +221,20 @@ def dsv4_o_proj(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.T
         workspace = torch.empty(need, dtype=torch.uint8, device=o.device)
     if out is None:
         out = torch.empty((T, hidden), dtype=torch.bfloat16, device=o.device)
-    rc = lib.dsv4_o_proj(o.data_ptr(), positions.data_ptr(), cos_sin_cache.data_ptr(),
-                         cos_sin_cache.shape[0], T, n_groups, heads_per_group, nope_dim, rope_dim,
-                         quant_group_size, o_lora_rank, hidden, wo_a.data_ptr(),
-                         wo_a_scale.data_ptr(), wo_b.data_ptr(), wo_b_scale.data_ptr(),
-                         out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(stream))
+    args = (o.data_ptr(), positions.data_ptr(), cos_sin_cache.data_ptr(), cos_sin_cache.shape[0],
+            T, n_groups, heads_per_group, nope_dim, rope_dim, quant_group_size, o_lora_rank,
+            hidden, wo_a.data_ptr(), wo_a_scale.data_ptr(), wo_b.data_ptr(),
+            wo_b_scale.data_ptr(), out.data_ptr(), workspace.data_ptr(), workspace.numel())
+    if stage_events is None:
+        rc = lib.dsv4_o_proj(*args, _stream(stream))
+    else:
+        if len(stage_events) != 4:
+            raise ValueError("stage_events must hold 4 events")
+        for ev in stage_events:
+            if not ev.cuda_event:   # torch creates the event on its first record
+                ev.record(torch.cuda.current_stream() if stream is None else stream)
+        handles = (ctypes.c_void_p * 4)(*[ev.cuda_event for ev in stage_events])
+        rc = lib.dsv4_o_proj_with_events(*args, handles, _stream(stream))
     _check(rc, "dsv4_o_proj")
     return out
 

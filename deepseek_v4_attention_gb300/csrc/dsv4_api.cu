@@ -190,6 +190,20 @@ int dsv4_o_proj(const void* o, const int64_t* positions, const float* cos_sin_ca
                 const void* wo_a_fp8, const uint8_t* wo_a_scale, const void* wo_b_fp8,
                 const uint8_t* wo_b_scale, void* out, void* workspace, size_t workspace_bytes,
                 void* stream) {
+  return dsv4_o_proj_with_events(o, positions, cos_sin_cache, max_pos, num_tokens, n_groups,
+                                 heads_per_group, nope_dim, rope_dim, quant_group_size,
+                                 o_lora_rank, hidden, wo_a_fp8, wo_a_scale, wo_b_fp8, wo_b_scale,
+                                 out, workspace, workspace_bytes, nullptr, stream);
+}
+
+int dsv4_o_proj_with_events(const void* o, const int64_t* positions, const float* cos_sin_cache,
+                            int64_t max_pos, int64_t num_tokens, int n_groups,
+                            int heads_per_group, int nope_dim, int rope_dim,
+                            int quant_group_size, int o_lora_rank, int hidden,
+                            const void* wo_a_fp8, const uint8_t* wo_a_scale,
+                            const void* wo_b_fp8, const uint8_t* wo_b_scale, void* out,
+                            void* workspace, size_t workspace_bytes, void* const* stage_events,
+                            void* stream) {
   t_last_launches = 0;
   int rc = check_quant_shapes(num_tokens, max_pos, n_groups, heads_per_group, nope_dim, rope_dim,
                               quant_group_size);
@@ -229,9 +243,15 @@ int dsv4_o_proj(const void* o, const int64_t* positions, const float* cos_sin_ca
   ws += round256(static_cast<size_t>(T) * C);
   int32_t* zs = reinterpret_cast<int32_t*>(ws);
 
+  auto mark = [&](int i) {
+    if (!stage_events) return true;
+    return cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s) == cudaSuccess;
+  };
+  if (!mark(0)) return DSV4_ERR_CUDA;
   rc = launch_inv_rope_fp8_quant(o, positions, cos_sin_cache, T, max_pos, n_groups,
                                  heads_per_group, x, xs, s, dev);
   if (rc != DSV4_OK) return rc;
+  if (!mark(1)) return DSV4_ERR_CUDA;
 
   GemmProblem a;
   a.T = T;
@@ -246,6 +266,7 @@ int dsv4_o_proj(const void* o, const int64_t* positions, const float* cos_sin_ca
   a.q_out = zq;
   a.q_scale = zs;
   if ((rc = launch_block_scaled_gemm(a, s, dev)) != DSV4_OK) return rc;
+  if (!mark(2)) return DSV4_ERR_CUDA;
 
   GemmProblem b;
   b.T = T;
@@ -259,6 +280,7 @@ int dsv4_o_proj(const void* o, const int64_t* positions, const float* cos_sin_ca
   b.epilogue = kEpiBf16;
   b.out_bf16 = out;
   if ((rc = launch_block_scaled_gemm(b, s, dev)) != DSV4_OK) return rc;
+  if (!mark(3)) return DSV4_ERR_CUDA;
   t_last_launches = 3;
   return DSV4_OK;
 }

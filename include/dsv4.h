@@ -149,6 +149,23 @@ int dsv4_o_proj(const void* o, const int64_t* positions, const float* cos_sin_ca
                 const uint8_t* wo_b_scale, void* out, void* workspace, size_t workspace_bytes,
                 void* stream);
 
+/*
+ * dsv4_o_proj, and in addition records four caller-created CUDA events
+ * (cudaEvent_t handles) on `stream`: stage_events[0] before the quantisation
+ * kernel and stage_events[1..3] after the quantisation, wo_a and wo_b kernels.
+ * Elapsed times between consecutive events are the per-kernel device times of
+ * the step, measured without a profiler.  stage_events == NULL behaves exactly
+ * like dsv4_o_proj.  DSV4_ERR_CUDA if an event record fails.
+ */
+int dsv4_o_proj_with_events(const void* o, const int64_t* positions, const float* cos_sin_cache,
+                            int64_t max_pos, int64_t num_tokens, int n_groups,
+                            int heads_per_group, int nope_dim, int rope_dim,
+                            int quant_group_size, int o_lora_rank, int hidden,
+                            const void* wo_a_fp8, const uint8_t* wo_a_scale,
+                            const void* wo_b_fp8, const uint8_t* wo_b_scale, void* out,
+                            void* workspace, size_t workspace_bytes, void* const* stage_events,
+                            void* stream);
+
 /* Human-readable name of a dsv4_status value (static string). */
 const char* dsv4_status_string(int status);
 

@@ -47,6 +47,7 @@ def _load():
         P = ctypes.c_void_p
         I64 = ctypes.c_int64
         sig = {
+            "oracle_num_threads": (ctypes.c_int, []),
             "oracle_bf16_to_float": (ctypes.c_float, [ctypes.c_uint16]),
             "oracle_bf16_from_double": (ctypes.c_uint16, [ctypes.c_double]),
             "oracle_e4m3_decode": (ctypes.c_double, [ctypes.c_uint8]),
@@ -101,6 +102,10 @@ class OracleError(RuntimeError):
 def _check(rc: int, what: str):
     if rc != OK:
         raise OracleError(rc, what)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
 
 
 # -- number formats -------------------------------------------------------------

@@ -35,6 +35,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define OR_OK 0
 #define OR_ERR_SHAPE (-1)
@@ -49,6 +52,16 @@
  * all-zero blocks; this reading keeps the UE8M0 byte finite (it gives 105,
  * i.e. 2^-22, for an all-zero block). */
 #define AMAX_FLOOR 1e-4f
+
+/* Threads the oracle's parallel loops use (for reporting its timings). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------------ */
 /* Number formats                                                            */

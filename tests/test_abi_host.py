@@ -19,7 +19,8 @@ def lib():
 def test_exports_every_header_function(lib):
     names = k.header_functions()
     assert set(names) == {"dsv4_inv_rope_fp8_quant", "dsv4_grouped_wo_a",
-                          "dsv4_o_proj_workspace_bytes", "dsv4_o_proj", "dsv4_status_string",
+                          "dsv4_o_proj_workspace_bytes", "dsv4_o_proj", "dsv4_o_proj_with_events",
+                          "dsv4_status_string",
                           "dsv4_device_status", "dsv4_last_launch_count"}
     out = subprocess.run(["nm", "-D", "--defined-only", k.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
