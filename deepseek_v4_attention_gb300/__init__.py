@@ -63,6 +63,8 @@ def load_library() -> ctypes.CDLL:
     lib.dsv4_o_proj_with_events.argtypes = [P, P, P, I64, I64, I, I, I, I, I, I, I, P, P, P, P,
                                             P, P, ctypes.c_size_t, P, P]
     lib.dsv4_o_proj_with_events.restype = I
+    lib.dsv4_o_proj_static.argtypes = [P, P, P, I64, I64, I, I, I, I, I, I, I, P, P, P, P, P, P]
+    lib.dsv4_o_proj_static.restype = I
     lib.dsv4_status_string.argtypes = [I]
     lib.dsv4_status_string.restype = ctypes.c_char_p
     lib.dsv4_device_status.argtypes = [P, I]
@@ -236,6 +238,30 @@ def dsv4_o_proj(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.T
         handles = (ctypes.c_void_p * 4)(*[ev.cuda_event for ev in stage_events])
         rc = lib.dsv4_o_proj_with_events(*args, handles, _stream(stream))
     _check(rc, "dsv4_o_proj")
+    return out
+
+
+STATIC_SCRATCH_BYTES = 64 << 20   # DSV4_STATIC_SCRATCH_BYTES in include/dsv4.h
+
+
+def dsv4_o_proj_static(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                       wo_a: torch.Tensor, wo_a_scale: torch.Tensor, wo_b: torch.Tensor,
+                       wo_b_scale: torch.Tensor, *, n_groups: int, heads_per_group: int,
+                       o_lora_rank: int, out: torch.Tensor, nope_dim: int = 448,
+                       rope_dim: int = 64, quant_group_size: int = 128,
+                       stream=None) -> torch.Tensor:
+    """dsv4_o_proj for callers that cannot allocate device memory: the library
+    uses its own fixed scratch (STATIC_SCRATCH_BYTES) and this wrapper
+    allocates nothing either, so `out` must be given.  Calls that overlap on
+    the GPU share that scratch and race."""
+    lib = load_library()
+    T, H, hd = o.shape
+    rc = lib.dsv4_o_proj_static(o.data_ptr(), positions.data_ptr(), cos_sin_cache.data_ptr(),
+                                cos_sin_cache.shape[0], T, n_groups, heads_per_group, nope_dim,
+                                rope_dim, quant_group_size, o_lora_rank, wo_b.shape[0],
+                                wo_a.data_ptr(), wo_a_scale.data_ptr(), wo_b.data_ptr(),
+                                wo_b_scale.data_ptr(), out.data_ptr(), _stream(stream))
+    _check(rc, "dsv4_o_proj_static")
     return out
 
 

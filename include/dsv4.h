@@ -166,6 +166,49 @@ int dsv4_o_proj_with_events(const void* o, const int64_t* positions, const float
                             void* workspace, size_t workspace_bytes, void* const* stage_events,
                             void* stream);
 
+/*
+ * Size of the library's own scratch for dsv4_o_proj_static: 64 MiB, held on
+ * every device that loads this library until the process exits.  It covers
+ * dsv4_o_proj_workspace_bytes() up to this value, e.g. up to 812 tokens of the
+ * 128-head, o_lora_rank 1024 configuration (82.5 KB per token).
+ */
+#define DSV4_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * dsv4_o_proj without a workspace argument and without any allocation.  The
+ * pages have no counterpart to this entry point.
+ *
+ * For callers that cannot allocate device memory at call time: a C program or
+ * plugin running inside an engine that owns all device memory through its own
+ * pre-planned pool and gives the plugin no allocator, or code on a latency
+ * path where cudaMalloc/cudaFree would synchronise the device and stall other
+ * streams.  The scratch that dsv4_o_proj takes from the caller (the quantised
+ * groups, the re-quantised z and their scales) lives instead in one file-scope
+ * device array of DSV4_STATIC_SCRATCH_BYTES inside this library.  The caller
+ * still passes and owns every input and output.  The call allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Arguments, layouts and errors are those of dsv4_o_proj.  In addition it
+ * returns DSV4_ERR_WORKSPACE, launching nothing, when
+ * dsv4_o_proj_workspace_bytes() for these sizes exceeds
+ * DSV4_STATIC_SCRATCH_BYTES.
+ *
+ * The first call on a device looks up the device address of the array
+ * (cudaGetSymbolAddress, once per device, with that device current); make
+ * that first call before any stream capture.  Every call on a device uses the
+ * same array, and the array keeps the last call's contents: calls that overlap
+ * on the GPU (on different streams, or from different host threads without
+ * ordering) race on it and must be serialised by the caller.  Nothing in the
+ * array needs to start at zero: every byte a kernel reads was written earlier
+ * in the same call.
+ */
+int dsv4_o_proj_static(const void* o, const int64_t* positions, const float* cos_sin_cache,
+                       int64_t max_pos, int64_t num_tokens, int n_groups, int heads_per_group,
+                       int nope_dim, int rope_dim, int quant_group_size, int o_lora_rank,
+                       int hidden, const void* wo_a_fp8, const uint8_t* wo_a_scale,
+                       const void* wo_b_fp8, const uint8_t* wo_b_scale, void* out,
+                       void* stream);
+
 /* Human-readable name of a dsv4_status value (static string). */
 const char* dsv4_status_string(int status);
 

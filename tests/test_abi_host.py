@@ -20,6 +20,7 @@ def test_exports_every_header_function(lib):
     names = k.header_functions()
     assert set(names) == {"dsv4_inv_rope_fp8_quant", "dsv4_grouped_wo_a",
                           "dsv4_o_proj_workspace_bytes", "dsv4_o_proj", "dsv4_o_proj_with_events",
+                          "dsv4_o_proj_static",
                           "dsv4_status_string",
                           "dsv4_device_status", "dsv4_last_launch_count"}
     out = subprocess.run(["nm", "-D", "--defined-only", k.LIB_PATH], capture_output=True,
@@ -101,3 +102,17 @@ def test_o_proj_host_validation_without_gpu(lib):
     for idx in (0, 1, 2, 12, 13, 14, 15, 16):
         a = list(good); a[idx] = None
         assert f(*a) == -2, idx
+
+
+def test_o_proj_static_host_validation_without_gpu(lib):
+    f = lib.dsv4_o_proj_static
+    P = 4096
+    good = [P, P, P, 65536, 64, 16, 8, 448, 64, 128, 1024, 7168, P, P, P, P, P, None]
+    a = list(good); a[4] = -1
+    assert f(*a) == -1
+    a = list(good); a[4] = 0
+    assert f(*a) == 0 and k.dsv4_last_launch_count() == 0
+    a = list(good); a[4] = 813          # beyond the fixed scratch: rejected before any CUDA call
+    assert f(*a) == -5
+    a = list(good); a[16] = None
+    assert f(*a) == -2
