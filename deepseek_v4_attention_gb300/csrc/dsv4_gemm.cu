@@ -7,7 +7,8 @@
 //
 //   C[t, g*N + n] = sum_k A[g][t][k] 2^ea[g][t][k/128] * B[g*N+n][k] 2^eb[(g*N+n)/128][k/128]
 //
-// Persistent, warp-specialised CTA of 192 threads, one CTA per SM:
+// Persistent, warp-specialised CTA, one per SM (tile 128 x kBN x 128, kBN = 128
+// or 256, see Cfg):
 //   warp 0     TMA producer: A tile (128 tokens x 128 k, 128B swizzle),
 //              B tile (128 rows x 128 k), the A scale words of the k-block
 //              (512 B, MN-major as the quantiser writes them); the B scales
@@ -17,11 +18,11 @@
 //              TMEM) and 4 tcgen05.mma (K = 32 each) per k-block; the whole
 //              warp first reorders the A scale words into the 32 x 16-byte
 //              layout that tcgen05.cp.32x128b.warpx4 expects.
-//   warps 2-5  epilogue: tcgen05.ld the 128 x 128 fp32 accumulator (each
-//              thread one row), then bf16 stores or the fused per-128 FP8
-//              re-quantisation.
-// TMEM: two 128-column accumulators (the epilogue of tile i overlaps the
-// MMAs of tile i+1) + 8 scale-factor columns per pipeline stage.
+//   warps 2-   epilogue: tcgen05.ld a 128-row x 128-column slice of the fp32
+//              accumulator per warp group (each thread one row), release the
+//              accumulator, then bf16 stores or the fused per-128 FP8
+//              re-quantisation (one thread holds one whole 128-block).
+// TMEM: the accumulator(s) + (4 + kBN/32) scale-factor columns per stage.
 //
 // Scale factors and the K = 128 blocks: the hardware applies one UE8M0 scale
 // per 32 k (scale_vec::1X).  A 128-wide k-block is issued as four K = 32 MMAs
@@ -39,33 +40,40 @@ namespace dsv4 {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBN = 128;
 constexpr int kBK = 128;
-constexpr int kStages = 6;
-constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
-constexpr int kAccCols = 2 * kBN;          // two accumulators
-constexpr int kSfCol0 = kAccCols;          // scale factors after the accumulators
-constexpr int kSfColsPerStage = 8;         // 4 for A (128 rows), 4 for B (128 rows)
-static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 
 constexpr uint32_t kABytes = kBM * kBK;    // 16 KiB
-constexpr uint32_t kBBytes = kBN * kBK;    // 16 KiB
 constexpr uint32_t kSfaBytes = kBM * 4;    // 512 B
-constexpr uint32_t kSfbBytes = kBN * 4;    // 512 B
 
-struct SmemPlan {
+// Tile configuration.  kBN = 128: two 128-column TMEM accumulators (the
+// epilogue of tile i overlaps the MMAs of tile i+1), 4 epilogue warps.
+// kBN = 256: one 256-column accumulator (N = 256 is the full-width single-SM
+// MMA), 8 epilogue warps that copy it to registers and release TMEM before
+// they convert and store, so the next tile's MMAs start almost at once.
+template <int kBN>
+struct Cfg {
+  static constexpr int kStages = (kBN == 128) ? 6 : 4;
+  static constexpr int kAccBufs = (kBN == 128) ? 2 : 1;
+  static constexpr int kEpiWarps = (kBN == 128) ? 4 : 8;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr uint32_t kBBytes = kBN * kBK;
+  static constexpr uint32_t kSfbBytes = kBN * 4;
+  static constexpr int kSfCol0 = kAccBufs * kBN;              // after the accumulators
+  static constexpr int kSfColsPerStage = 4 + kBN / 32;        // A: 4, B: kBN/32
+  static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+  // shared memory plan (operand tiles 1024-byte aligned for the 128B swizzle)
   static constexpr uint32_t a = 0;
   static constexpr uint32_t b = a + kStages * kABytes;
   static constexpr uint32_t sfa = b + kStages * kBBytes;
   static constexpr uint32_t sfb = sfa + kStages * kSfaBytes;
   static constexpr uint32_t bars = sfb + kStages * kSfbBytes;
-  // full[kStages], empty[kStages], tmem_full[2], tmem_empty[2], drain
-  static constexpr uint32_t n_bars = 2 * kStages + 5;
+  // full[kStages], empty[kStages], tmem_full[kAccBufs], tmem_empty[kAccBufs], drain
+  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 1;
   static constexpr uint32_t misc = bars + n_bars * 8;  // tmem base, abort flag
   static constexpr uint32_t total = misc + 16;
+  static constexpr uint32_t smem_bytes = total + 1024;  // + alignment slack
 };
-constexpr uint32_t kSmemBytes = SmemPlan::total + 1024;  // + alignment slack
 
 struct Params {
   int64_t T;
@@ -101,24 +109,29 @@ __device__ __forceinline__ uint32_t b_scale_word(const Params& p, int rb, int j)
   return w;
 }
 
-template <int kEpi>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kBN, int kEpi>
+__global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b,
                              const __grid_constant__ CUtensorMap tm_sfa, const Params p) {
+  using C = Cfg<kBN>;
+  constexpr int kStages = C::kStages;
+  constexpr int kAccBufs = C::kAccBufs;
+  constexpr uint32_t kBBytes = C::kBBytes;
+  constexpr uint32_t kSfbBytes = C::kSfbBytes;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128B-swizzled operand tiles
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemPlan::bars);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::bars);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tmem_full = bars + 2 * kStages;
-  uint64_t* tmem_empty = bars + 2 * kStages + 2;
-  uint64_t* drain = bars + 2 * kStages + 4;
-  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + SmemPlan::misc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemPlan::misc + 4);
+  uint64_t* tmem_empty = bars + 2 * kStages + kAccBufs;
+  uint64_t* drain = bars + 2 * kStages + 2 * kAccBufs;
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::misc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -128,9 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kAccBufs; ++a) {
       mbar_init(&tmem_full[a], 1);
-      mbar_init(&tmem_empty[a], 4);
+      mbar_init(&tmem_empty[a], C::kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -161,47 +174,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int packs = (p.k_blocks + 3) / 4;
     bool ok = true;
     // weight-scale words of the first tile, loaded ahead (lane j holds packs j, j+32, ...)
-    uint32_t wnext[4] = {0, 0, 0, 0};
+    constexpr int kRb = kBN / 128;   // 128-row weight-scale blocks per tile
+    uint32_t wnext[kRb][4];
+#pragma unroll
+    for (int r = 0; r < kRb; ++r)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) wnext[r][i] = 0u;
     if (blockIdx.x < p.num_tiles) {
       int g, nb, mb;
       tile_coords(p, blockIdx.x, g, nb, mb);
       const int rb = (g * p.N + nb * kBN) / 128;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (lane + 32 * i < packs) wnext[i] = b_scale_word(p, rb, lane + 32 * i);
+      for (int r = 0; r < kRb; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (lane + 32 * i < packs) wnext[r][i] = b_scale_word(p, rb + r, lane + 32 * i);
     }
     for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
       int g, n_blk, m_blk;
       tile_coords(p, tile, g, n_blk, m_blk);
-      uint32_t wcur[4];
+      uint32_t wcur[kRb][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) wcur[i] = wnext[i];
+      for (int r = 0; r < kRb; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) wcur[r][i] = wnext[r][i];
       const int next = tile + gridDim.x;
       if (next < p.num_tiles) {
         int g2, nb2, mb2;
         tile_coords(p, next, g2, nb2, mb2);
         const int rb2 = (g2 * p.N + nb2 * kBN) / 128;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          wnext[i] = (lane + 32 * i < packs) ? b_scale_word(p, rb2, lane + 32 * i) : 0u;
+        for (int r = 0; r < kRb; ++r)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            wnext[r][i] = (lane + 32 * i < packs) ? b_scale_word(p, rb2 + r, lane + 32 * i) : 0u;
       }
       const int m0 = m_blk * kBM;
       const int brow = g * p.N + n_blk * kBN;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        // B scale-factor tile: 128 rows share the byte of their 128-row block
+        // B scale-factor tile: each 128-row block's rows share its byte
         const int j = kb >> 2;
-        const uint32_t src = (j < 32) ? wcur[0] : (j < 64) ? wcur[1] : (j < 96) ? wcur[2] : wcur[3];
-        const uint32_t word = __shfl_sync(0xFFFFFFFFu, src, j & 31);
-        uint4* sfb = reinterpret_cast<uint4*>(smem + SmemPlan::sfb + stage * kSfbBytes);
-        sfb[lane] = make_uint4(word, word, word, word);
+        uint4* sfb = reinterpret_cast<uint4*>(smem + C::sfb + stage * kSfbBytes);
+#pragma unroll
+        for (int r = 0; r < kRb; ++r) {
+          const uint32_t src = (j < 32) ? wcur[r][0] : (j < 64) ? wcur[r][1]
+                             : (j < 96) ? wcur[r][2] : wcur[r][3];
+          const uint32_t word = __shfl_sync(0xFFFFFFFFu, src, j & 31);
+          sfb[32 * r + lane] = make_uint4(word, word, word, word);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + kSfaBytes);
-          tma_load_3d(smem + SmemPlan::a + stage * kABytes, &tm_a, &full[stage], kb * kBK, m0, g);
-          tma_load_2d(smem + SmemPlan::b + stage * kBBytes, &tm_b, &full[stage], kb * kBK, brow);
-          tma_load_3d(smem + SmemPlan::sfa + stage * kSfaBytes, &tm_sfa, &full[stage], m0, j, g);
+          tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBK, m0, g);
+          tma_load_2d(smem + C::b + stage * kBBytes, &tm_b, &full[stage], kb * kBK, brow);
+          tma_load_3d(smem + C::sfa + stage * kSfaBytes, &tm_sfa, &full[stage], m0, j, g);
         }
         issued[stage] = true;
         issued_parity[stage] = phase;
@@ -228,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_warp(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         // reorder the 128 A scale words: row m = 32 i + r goes to word 4 r + i
-        uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + SmemPlan::sfa + stage * kSfaBytes);
+        uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + C::sfa + stage * kSfaBytes);
         uint32_t v0 = sfa[lane], v1 = sfa[32 + lane], v2 = sfa[64 + lane], v3 = sfa[96 + lane];
         __syncwarp();
         reinterpret_cast<uint4*>(sfa)[lane] = make_uint4(v0, v1, v2, v3);
@@ -236,13 +264,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           const uint32_t sf_col =
-              tmem_base + static_cast<uint32_t>(kSfCol0 + stage * kSfColsPerStage);
+              tmem_base + static_cast<uint32_t>(C::kSfCol0 + stage * C::kSfColsPerStage);
           const uint32_t sfa_addr = smem_addr(sfa);
-          const uint32_t sfb_addr = smem_addr(smem + SmemPlan::sfb + stage * kSfbBytes);
+          const uint32_t sfb_addr = smem_addr(smem + C::sfb + stage * kSfbBytes);
           tmem_cp_32x128b_x4(sf_col, smem_desc(sfa_addr, 0, 128, 0));
-          tmem_cp_32x128b_x4(sf_col + 4, smem_desc(sfb_addr, 0, 128, 0));
-          const uint32_t a_addr = smem_addr(smem + SmemPlan::a + stage * kABytes);
-          const uint32_t b_addr = smem_addr(smem + SmemPlan::b + stage * kBBytes);
+#pragma unroll
+          for (int r = 0; r < kBN / 128; ++r)
+            tmem_cp_32x128b_x4(sf_col + 4 + 4 * r, smem_desc(sfb_addr + 512 * r, 0, 128, 0));
+          const uint32_t a_addr = smem_addr(smem + C::a + stage * kABytes);
+          const uint32_t b_addr = smem_addr(smem + C::b + stage * kBBytes);
           const uint32_t id = static_cast<uint32_t>(kb & 3);
           const uint32_t idesc = mxf8_idesc(kBM, kBN, id, id);
 #pragma unroll
@@ -259,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (lane == 0) mma_commit(&tmem_full[acc]);
       __syncwarp();
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
     }
     if (*abort_flag && lane == 0) {
       // let every MMA / copy this thread issued finish before TMEM is freed
@@ -268,7 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int epi = warp - 2;             // 0 .. kEpiWarps-1
+    const int quarter = warp & 3;         // TMEM lanes this warp may access
+    const int col_half = epi >> 2;        // which 128 columns of the tile
     const int row = quarter * 32 + lane;
     const int64_t ld = static_cast<int64_t>(p.G) * p.N;
     int acc = 0;
@@ -280,41 +312,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t t = static_cast<int64_t>(m_blk) * kBM + row;
       const bool live = t < p.T;
-      const int64_t col0 = static_cast<int64_t>(g) * p.N + static_cast<int64_t>(n_blk) * kBN;
+      const int64_t col0 = static_cast<int64_t>(g) * p.N + static_cast<int64_t>(n_blk) * kBN +
+                           128 * col_half;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                             static_cast<uint32_t>(acc * kBN);
-      if constexpr (kEpi == kEpiBf16) {
+                             static_cast<uint32_t>(acc * kBN + 128 * col_half);
+      // the whole 128-column slice to registers, then hand the accumulator back
+      uint32_t r[4][32];
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32cols(taddr + 32u * c, r);
-          tmem_ld_wait();
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + t * ld + col0 + 32 * c);
+      for (int c = 0; c < 4; ++c) tmem_ld_32cols(taddr + 32u * c, r[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      if constexpr (kEpi == kEpiBf16) {
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + t * ld + col0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint32_t w[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * i]),
-                                                               __uint_as_float(r[8 * v + 2 * i + 1]));
+                const __nv_bfloat162 h = __floats2bfloat162_rn(
+                    __uint_as_float(r[c][8 * v + 2 * i]), __uint_as_float(r[c][8 * v + 2 * i + 1]));
                 w[i] = *reinterpret_cast<const uint32_t*>(&h);
               }
-              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[4 * c + v] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-          }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tmem_empty[acc]);
       } else {
-        uint32_t r[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_32cols(taddr + 32u * c, r[c]);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tmem_empty[acc]);  // accumulator is in registers now
         // z is a bf16 tensor: round first, then quantise the rounded values
         float amax = 0.f;
 #pragma unroll
@@ -365,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           sbytes[((blk >> 2) * p.t_al + t) * 4 + (blk & 3)] = static_cast<uint8_t>(e + 127);
         }
       }
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
     }
   }
 
@@ -407,14 +434,15 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kEpi>
+template <int kBN, int kEpi>
 int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
+  using C = Cfg<kBN>;
   static int configured_for[64] = {0};
   if (dev.device < 0 || dev.device >= 64) return DSV4_ERR_UNSUPPORTED;
   if (!configured_for[dev.device]) {
-    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kEpi>,
+    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+                             static_cast<int>(C::smem_bytes)) != cudaSuccess)
       return DSV4_ERR_CUDA;
     configured_for[dev.device] = 1;
   }
@@ -470,7 +498,8 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   p.status = dev.status;
 
   const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
-  block_scaled_gemm_kernel<kEpi><<<grid, kThreads, kSmemBytes, stream>>>(tm_a, tm_b, tm_sfa, p);
+  block_scaled_gemm_kernel<kBN, kEpi>
+      <<<grid, C::kThreads, C::smem_bytes, stream>>>(tm_a, tm_b, tm_sfa, p);
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
@@ -478,8 +507,16 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
 
 int launch_block_scaled_gemm(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
   if (q.K / 128 > 4 * 32 * 4) return DSV4_ERR_UNSUPPORTED;  // weight-scale words held per lane
-  if (q.epilogue == kEpiQuant) return launch_impl<kEpiQuant>(q, stream, dev);
-  return launch_impl<kEpiBf16>(q, stream, dev);
+  // 256-wide tiles when they divide N and still give every SM a tile;
+  // otherwise 128-wide tiles (twice the CTAs, for the small decode shapes)
+  const int64_t m_tiles = (q.T + kBM - 1) / kBM;
+  const bool wide = q.N % 256 == 0 && m_tiles * (q.N / 256) * q.G >= dev.num_sms;
+  if (wide) {
+    if (q.epilogue == kEpiQuant) return launch_impl<256, kEpiQuant>(q, stream, dev);
+    return launch_impl<256, kEpiBf16>(q, stream, dev);
+  }
+  if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant>(q, stream, dev);
+  return launch_impl<128, kEpiBf16>(q, stream, dev);
 }
 
 }  // namespace dsv4

@@ -27,8 +27,10 @@ def _gpu_wo_a(x, xs, w, ws, T, G, D, R, dev):
     return to_bits(z)
 
 
+# the last case takes the 256-wide tile path (>= one tile per SM), the others 128-wide
 @pytest.mark.parametrize("T,G,D,R", [(16, 2, 1024, 128), (64, 8, 4096, 1024), (1, 1, 128, 128),
-                                     (3, 2, 512, 256), (129, 3, 640, 384), (200, 1, 1024, 896)])
+                                     (3, 2, 512, 256), (129, 3, 640, 384), (200, 1, 1024, 896),
+                                     (1200, 4, 640, 1024)])
 def test_grouped_wo_a_random_operands(dev, T, G, D, R):
     T_al = oracle.tma_aligned_tokens(T)
     x, xs = di.random_fp8_activation(T, G, D, seed=T * 7 + G, tma_aligned_T=T_al)
@@ -39,9 +41,9 @@ def test_grouped_wo_a_random_operands(dev, T, G, D, R):
     assert err <= GEMM_RTOL, err
 
 
-def test_grouped_wo_a_identity_weight_is_exact(dev):
+@pytest.mark.parametrize("T,G,D,R", [(130, 2, 512, 256), (1200, 16, 512, 256)])
+def test_grouped_wo_a_identity_weight_is_exact(dev, T, G, D, R):
     """W = I in every group with unit scales: z must equal bf16(dq_x) exactly."""
-    T, G, D, R = 130, 2, 512, 256
     T_al = oracle.tma_aligned_tokens(T)
     x, xs = di.random_fp8_activation(T, G, D, seed=5, tma_aligned_T=T_al)
     w = torch.zeros(G * R, D, dtype=torch.uint8)
@@ -53,10 +55,12 @@ def test_grouped_wo_a_identity_weight_is_exact(dev):
     assert np.array_equal(zg, zr)
 
 
-def test_grouped_wo_a_scale_rows(dev):
-    """Scales that vary only by token row, and only by k-block: catches a wrong
-    scale-factor layout in tensor memory (exact products, exact sums)."""
-    T, G, D, R = 128, 1, 1024, 128
+@pytest.mark.parametrize("T,G,R", [(128, 1, 128), (1280, 16, 256)])
+def test_grouped_wo_a_scale_rows(dev, T, G, R):
+    """Scales that vary only by token row, by k-block and by 128-row weight
+    block: catches a wrong scale-factor layout in tensor memory (exact products,
+    exact sums)."""
+    D = 1024
     T_al = T
     codes = torch.full((G, T, D), 0x38, dtype=torch.uint8)          # all ones
     b = torch.zeros((G, 8, T_al), dtype=torch.int64)
@@ -65,9 +69,10 @@ def test_grouped_wo_a_scale_rows(dev):
         b[:, kb, :] = 120 + row_e + kb                              # + per-block exponent
     words = (b[:, 0::4] | (b[:, 1::4] << 8) | (b[:, 2::4] << 16) | (b[:, 3::4] << 24))
     words = torch.where(words >= 2 ** 31, words - 2 ** 32, words).to(torch.int32)
-    w = torch.full((R, D), 0x38, dtype=torch.uint8)
-    ws = torch.full((1, 8), 127, dtype=torch.uint8)
-    ws[0, 3] = 125
+    w = torch.full((G * R, D), 0x38, dtype=torch.uint8)
+    ws = torch.full((G * R // 128, 8), 127, dtype=torch.uint8)
+    ws[:, 3] = 125
+    ws[1::2, 5] = 129                                                # odd 128-row blocks differ
     zg = _gpu_wo_a(codes, words, w, ws, T, G, D, R, dev)
     zr = oracle.grouped_gemm(codes, words, w, ws, T, G, D, R)
     assert np.array_equal(zg, zr)
