@@ -14,10 +14,12 @@
 //              (512 B, MN-major as the quantiser writes them); the B scales
 //              are one UE8M0 byte per (128-row block, k-block), expanded here
 //              into the 128-row scale-factor tile.
-//   warp 1     allocates TMEM; one lane issues tcgen05.cp (scale factors ->
-//              TMEM) and 4 tcgen05.mma (K = 32 each) per k-block; the whole
-//              warp first reorders the A scale words into the 32 x 16-byte
-//              layout that tcgen05.cp.32x128b.warpx4 expects.
+//   warp 1     allocates TMEM; one lane issues 4 tcgen05.mma (K = 32 each) per
+//              k-block and, once per 4 k-blocks (one packed int32 of scales),
+//              tcgen05.cp of the scale factors into a TMEM slot; the whole warp
+//              first reorders the A scale words into the 32 x 16-byte layout
+//              that tcgen05.cp.32x128b.warpx4 expects.  A slot is rewritten
+//              only after a commit barrier shows the MMAs reading it are done.
 //   warps 2-   epilogue: tcgen05.ld a 128-row x 128-column slice of the fp32
 //              accumulator per warp group (each thread one row), release the
 //              accumulator, then bf16 stores or the fused per-128 FP8
@@ -59,17 +61,21 @@ struct Cfg {
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kBBytes = kBN * kBK;
   static constexpr uint32_t kSfbBytes = kBN * 4;
+  // Scale factors are staged once per 4 k-blocks (one packed int32 covers four
+  // 128-wide blocks) into one of kSfSlots TMEM slots of (4 + kBN/32) columns.
+  static constexpr int kSfSlots = 3;
   static constexpr int kSfCol0 = kAccBufs * kBN;              // after the accumulators
-  static constexpr int kSfColsPerStage = 4 + kBN / 32;        // A: 4, B: kBN/32
-  static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+  static constexpr int kSfColsPerSlot = 4 + kBN / 32;         // A: 4, B: kBN/32
+  static_assert(kSfCol0 + kSfSlots * kSfColsPerSlot <= kTmemCols, "TMEM budget");
   // shared memory plan (operand tiles 1024-byte aligned for the 128B swizzle)
   static constexpr uint32_t a = 0;
   static constexpr uint32_t b = a + kStages * kABytes;
   static constexpr uint32_t sfa = b + kStages * kBBytes;
   static constexpr uint32_t sfb = sfa + kStages * kSfaBytes;
   static constexpr uint32_t bars = sfb + kStages * kSfbBytes;
-  // full[kStages], empty[kStages], tmem_full[kAccBufs], tmem_empty[kAccBufs], drain
-  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 1;
+  // full[kStages], empty[kStages], tmem_full[kAccBufs], tmem_empty[kAccBufs], drain,
+  // sf_free[kSfSlots]
+  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 1 + kSfSlots;
   static constexpr uint32_t misc = bars + n_bars * 8;  // tmem base, abort flag
   static constexpr uint32_t total = misc + 16;
   static constexpr uint32_t smem_bytes = total + 1024;  // + alignment slack
@@ -130,6 +136,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
   uint64_t* tmem_full = bars + 2 * kStages;
   uint64_t* tmem_empty = bars + 2 * kStages + kAccBufs;
   uint64_t* drain = bars + 2 * kStages + 2 * kAccBufs;
+  uint64_t* sf_free = drain + 1;
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::misc + 4);
 
@@ -146,6 +153,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
       mbar_init(&tmem_empty[a], C::kEpiWarps);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < C::kSfSlots; ++i) mbar_init(&sf_free[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -213,23 +221,28 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
       const int brow = g * p.N + n_blk * kBN;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        // B scale-factor tile: each 128-row block's rows share its byte
+        // scale factors only at the first k-block of each packed int32 (4 k-blocks)
         const int j = kb >> 2;
-        uint4* sfb = reinterpret_cast<uint4*>(smem + C::sfb + stage * kSfbBytes);
+        const bool pack_start = (kb & 3) == 0;
+        if (pack_start) {
+          // B scale-factor tile: each 128-row block's rows share its byte
+          uint4* sfb = reinterpret_cast<uint4*>(smem + C::sfb + stage * kSfbBytes);
 #pragma unroll
-        for (int r = 0; r < kRb; ++r) {
-          const uint32_t src = (j < 32) ? wcur[r][0] : (j < 64) ? wcur[r][1]
-                             : (j < 96) ? wcur[r][2] : wcur[r][3];
-          const uint32_t word = __shfl_sync(0xFFFFFFFFu, src, j & 31);
-          sfb[32 * r + lane] = make_uint4(word, word, word, word);
+          for (int r = 0; r < kRb; ++r) {
+            const uint32_t src = (j < 32) ? wcur[r][0] : (j < 64) ? wcur[r][1]
+                               : (j < 96) ? wcur[r][2] : wcur[r][3];
+            const uint32_t word = __shfl_sync(0xFFFFFFFFu, src, j & 31);
+            sfb[32 * r + lane] = make_uint4(word, word, word, word);
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + kSfaBytes);
+          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + (pack_start ? kSfaBytes : 0u));
           tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBK, m0, g);
           tma_load_2d(smem + C::b + stage * kBBytes, &tm_b, &full[stage], kb * kBK, brow);
-          tma_load_3d(smem + C::sfa + stage * kSfaBytes, &tm_sfa, &full[stage], m0, j, g);
+          if (pack_start)
+            tma_load_3d(smem + C::sfa + stage * kSfaBytes, &tm_sfa, &full[stage], m0, j, g);
         }
         issued[stage] = true;
         issued_parity[stage] = phase;
@@ -247,30 +260,45 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t packs_done = 0;  // scale-factor packs staged so far (all tiles)
     bool ok = true;
     for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
       if (!mbar_wait_warp(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+      uint32_t sf_col = 0;
+      int slot = 0;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         if (!mbar_wait_warp(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        // reorder the 128 A scale words: row m = 32 i + r goes to word 4 r + i
-        uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + C::sfa + stage * kSfaBytes);
-        uint32_t v0 = sfa[lane], v1 = sfa[32 + lane], v2 = sfa[64 + lane], v3 = sfa[96 + lane];
-        __syncwarp();
-        reinterpret_cast<uint4*>(sfa)[lane] = make_uint4(v0, v1, v2, v3);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t sf_col =
-              tmem_base + static_cast<uint32_t>(C::kSfCol0 + stage * C::kSfColsPerStage);
-          const uint32_t sfa_addr = smem_addr(sfa);
-          const uint32_t sfb_addr = smem_addr(smem + C::sfb + stage * kSfbBytes);
-          tmem_cp_32x128b_x4(sf_col, smem_desc(sfa_addr, 0, 128, 0));
+        if ((kb & 3) == 0) {
+          // a new pack of scale factors: wait until the MMAs that read this
+          // slot three packs ago have completed, then stage it
+          slot = static_cast<int>(packs_done % C::kSfSlots);
+          const uint32_t slot_phase = (packs_done / C::kSfSlots) & 1u;
+          if (!mbar_wait_warp(&sf_free[slot], slot_phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          ++packs_done;
+          // reorder the 128 A scale words: row m = 32 i + r goes to word 4 r + i
+          uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + C::sfa + stage * kSfaBytes);
+          uint32_t v0 = sfa[lane], v1 = sfa[32 + lane], v2 = sfa[64 + lane], v3 = sfa[96 + lane];
+          __syncwarp();
+          reinterpret_cast<uint4*>(sfa)[lane] = make_uint4(v0, v1, v2, v3);
+          fence_proxy_async_smem();
+          __syncwarp();
+          sf_col = tmem_base + static_cast<uint32_t>(C::kSfCol0 + slot * C::kSfColsPerSlot);
+          if (lane == 0) {
+            const uint32_t sfa_addr = smem_addr(sfa);
+            const uint32_t sfb_addr = smem_addr(smem + C::sfb + stage * kSfbBytes);
+            tmem_cp_32x128b_x4(sf_col, smem_desc(sfa_addr, 0, 128, 0));
 #pragma unroll
-          for (int r = 0; r < kBN / 128; ++r)
-            tmem_cp_32x128b_x4(sf_col + 4 + 4 * r, smem_desc(sfb_addr + 512 * r, 0, 128, 0));
+            for (int r = 0; r < kBN / 128; ++r)
+              tmem_cp_32x128b_x4(sf_col + 4 + 4 * r, smem_desc(sfb_addr + 512 * r, 0, 128, 0));
+          }
+        }
+        if (lane == 0) {
           const uint32_t a_addr = smem_addr(smem + C::a + stage * kABytes);
           const uint32_t b_addr = smem_addr(smem + C::b + stage * kBBytes);
           const uint32_t id = static_cast<uint32_t>(kb & 3);
@@ -282,6 +310,8 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
             mma_mxf8(d_tmem, ad, bd, idesc, sf_col, sf_col + 4, (kb | k) != 0 ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
+          // last k-block that reads this scale-factor slot: release it on completion
+          if ((kb & 3) == 3 || kb == p.k_blocks - 1) mma_commit(&sf_free[slot]);
         }
         __syncwarp();
         if (++stage == kStages) { stage = 0; phase ^= 1u; }

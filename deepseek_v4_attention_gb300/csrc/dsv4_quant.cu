@@ -17,9 +17,10 @@
 //     y1 = fma(b, c, -(a*s)), each cross product rounded first.
 //   - exponent from the fp32 bits of the amax (no log, no division);
 //     q = y * 2^-e is exact; cvt.rn.satfinite to e4m3.
-// Units are walked by a grid-stride loop in (t, h) order, so consecutive warps
-// stream consecutive KiB of o; kUnroll units are loaded before any is
-// processed to keep enough bytes in flight.
+// Work is walked by a grid-stride loop in (t, h) order, so consecutive warps
+// stream consecutive KiB of o; a warp takes kU heads of one token at a time,
+// loads all of them before using any, and reads the position and the cos/sin
+// row once for the kU heads.
 #include "dsv4_device.cuh"
 #include "dsv4_internal.h"
 
@@ -29,16 +30,6 @@ namespace {
 
 constexpr int kHeadDim = 512;
 constexpr int kRope = 64;
-constexpr int kUnroll = 2;
-
-struct Unit {
-  uint4 v0, v1;     // 8 bf16 each
-  float4 c, s;      // cos / sin of this lane's 4 pairs (lanes 24-31 only)
-  bool valid;
-  bool rotate;
-  int64_t t;
-  int h;
-};
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -75,6 +66,10 @@ __device__ __forceinline__ uint2 quant8(const float (&f)[8], float inv_scale) {
   return r;
 }
 
+// One warp iteration = kU consecutive heads of one token (H % kU == 0): the
+// position and the cos/sin row are loaded once for the kU heads, and all 2*kU
+// 16-byte loads of o are issued before any value is used.
+template <int kU>
 __global__ void __launch_bounds__(256) inv_rope_fp8_quant_kernel(
     const uint16_t* __restrict__ o, const int64_t* __restrict__ positions,
     const float* __restrict__ cache, int64_t T, int64_t max_pos, int H, int hpg,
@@ -83,50 +78,44 @@ __global__ void __launch_bounds__(256) inv_rope_fp8_quant_kernel(
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int64_t units = T * H;
+  const int64_t groups = T * (H / kU);  // (token, kU-head group) work items
   const int64_t D = static_cast<int64_t>(hpg) * kHeadDim;
   const bool rope_lane = lane >= 24;
-  const int pair0 = 4 * (lane - 24);  // first rope pair of this lane (lanes 24-31)
+  const int quad = lane - 24;  // lanes 24-31: rope pairs 4*quad .. 4*quad+3
 
-  for (int64_t base = warp * kUnroll; base < units; base += nwarps * kUnroll) {
-    Unit u[kUnroll];
-    // ---- issue every load of kUnroll units first
+  for (int64_t item = warp; item < groups; item += nwarps) {
+    const int64_t t = item / (H / kU);
+    const int h0 = static_cast<int>(item - t * (H / kU)) * kU;
+    const uint4* src = reinterpret_cast<const uint4*>(o + (t * H + h0) * kHeadDim);
+    uint4 v0[kU], v1[kU];
 #pragma unroll
-    for (int k = 0; k < kUnroll; ++k) {
-      const int64_t id = base + k;
-      u[k].valid = id < units;
-      u[k].t = u[k].valid ? id / H : 0;
-      u[k].h = u[k].valid ? static_cast<int>(id - u[k].t * H) : 0;
-      u[k].rotate = false;
-      if (u[k].valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(o + (u[k].t * H + u[k].h) * kHeadDim);
-        u[k].v0 = __ldcs(src + lane);
-        u[k].v1 = __ldcs(src + 32 + lane);
-        if (rope_lane) {
-          const int64_t p = __ldg(positions + u[k].t);
-          if (p >= 0 && p < max_pos) {
-            const float4* row = reinterpret_cast<const float4*>(cache + p * kRope);
-            u[k].c = __ldg(row + (pair0 >> 2));
-            u[k].s = __ldg(row + 8 + (pair0 >> 2));
-            u[k].rotate = true;
-          } else {
-            record_status(status, DSV4_ERR_RANGE);
-          }
-        }
+    for (int u = 0; u < kU; ++u) {
+      v0[u] = __ldcs(src + u * (kHeadDim / 8) + lane);
+      v1[u] = __ldcs(src + u * (kHeadDim / 8) + 32 + lane);
+    }
+    float4 c = make_float4(1.f, 1.f, 1.f, 1.f), sn = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool rotate = false;
+    if (rope_lane) {
+      const int64_t pos = __ldg(positions + t);
+      if (pos >= 0 && pos < max_pos) {
+        const float4* row = reinterpret_cast<const float4*>(cache + pos * kRope);
+        c = __ldg(row + quad);
+        sn = __ldg(row + 8 + quad);
+        rotate = true;
+      } else {
+        record_status(status, DSV4_ERR_RANGE);
       }
     }
-    // ---- rotate, reduce, quantise, store
 #pragma unroll
-    for (int k = 0; k < kUnroll; ++k) {
-      if (!u[k].valid) continue;  // warp-uniform
+    for (int u = 0; u < kU; ++u) {
       float f0[8], f1[8];
-      unpack8(u[k].v0, f0);
-      unpack8(u[k].v1, f1);
-      if (u[k].rotate) {
-        inv_rotate(f1[0], f1[1], u[k].c.x, u[k].s.x);
-        inv_rotate(f1[2], f1[3], u[k].c.y, u[k].s.y);
-        inv_rotate(f1[4], f1[5], u[k].c.z, u[k].s.z);
-        inv_rotate(f1[6], f1[7], u[k].c.w, u[k].s.w);
+      unpack8(v0[u], f0);
+      unpack8(v1[u], f1);
+      if (rotate) {
+        inv_rotate(f1[0], f1[1], c.x, sn.x);
+        inv_rotate(f1[2], f1[3], c.y, sn.y);
+        inv_rotate(f1[4], f1[5], c.z, sn.z);
+        inv_rotate(f1[6], f1[7], c.w, sn.w);
       }
       float m0 = 0.f, m1 = 0.f;
 #pragma unroll
@@ -141,9 +130,10 @@ __global__ void __launch_bounds__(256) inv_rope_fp8_quant_kernel(
       const uint2 q0 = quant8(f0, exp2_neg(e0));
       const uint2 q1 = quant8(f1, exp2_neg(e1));
 
-      const int g = u[k].h / hpg;
-      const int hh = u[k].h - g * hpg;
-      uint8_t* dst = out_fp8 + (static_cast<int64_t>(g) * T + u[k].t) * D +
+      const int h = h0 + u;
+      const int g = h / hpg;
+      const int hh = h - g * hpg;
+      uint8_t* dst = out_fp8 + (static_cast<int64_t>(g) * T + t) * D +
                      static_cast<int64_t>(hh) * kHeadDim;
       __stcs(reinterpret_cast<uint2*>(dst) + lane, q0);
       __stcs(reinterpret_cast<uint2*>(dst + 256) + lane, q1);
@@ -156,11 +146,26 @@ __global__ void __launch_bounds__(256) inv_rope_fp8_quant_kernel(
       const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, b2, 16);
       if (lane == 0) {
         const uint32_t word = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-        out_scale[(static_cast<int64_t>(g) * hpg + hh) * T_al + u[k].t] =
-            static_cast<int32_t>(word);
+        out_scale[(static_cast<int64_t>(g) * hpg + hh) * T_al + t] = static_cast<int32_t>(word);
       }
     }
   }
+}
+
+template <int kU>
+void launch_u(const void* o, const int64_t* positions, const float* cache, int64_t T,
+              int64_t max_pos, int H, int hpg, void* out_fp8, int32_t* out_scale,
+              cudaStream_t stream, const DeviceInfo& dev) {
+  const int64_t T_al = (T + 3) / 4 * 4;
+  const int threads = 256;
+  const int64_t items = T * (H / kU);
+  int64_t blocks = (items * 32 + threads - 1) / threads;
+  const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * (2048 / threads);
+  if (blocks > max_blocks) blocks = max_blocks;
+  if (blocks < 1) blocks = 1;
+  inv_rope_fp8_quant_kernel<kU><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      static_cast<const uint16_t*>(o), positions, cache, T, max_pos, H, hpg,
+      static_cast<uint8_t*>(out_fp8), out_scale, T_al, dev.status);
 }
 
 }  // namespace
@@ -170,17 +175,12 @@ int launch_inv_rope_fp8_quant(const void* o, const int64_t* positions, const flo
                               void* out_fp8, int32_t* out_scale, cudaStream_t stream,
                               const DeviceInfo& dev) {
   const int H = n_groups * hpg;
-  const int64_t units = T * H;
-  const int64_t T_al = (T + 3) / 4 * 4;
-  const int threads = 256;
-  const int64_t warps_needed = (units + kUnroll - 1) / kUnroll;
-  int64_t blocks = (warps_needed * 32 + threads - 1) / threads;
-  const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * (2048 / threads);
-  if (blocks > max_blocks) blocks = max_blocks;
-  if (blocks < 1) blocks = 1;
-  inv_rope_fp8_quant_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint16_t*>(o), positions, cache, T, max_pos, H, hpg,
-      static_cast<uint8_t*>(out_fp8), out_scale, T_al, dev.status);
+  if (H % 4 == 0)
+    launch_u<4>(o, positions, cache, T, max_pos, H, hpg, out_fp8, out_scale, stream, dev);
+  else if (H % 2 == 0)
+    launch_u<2>(o, positions, cache, T, max_pos, H, hpg, out_fp8, out_scale, stream, dev);
+  else
+    launch_u<1>(o, positions, cache, T, max_pos, H, hpg, out_fp8, out_scale, stream, dev);
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
