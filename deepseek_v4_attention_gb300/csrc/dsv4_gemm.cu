@@ -7,24 +7,28 @@
 //
 //   C[t, g*N + n] = sum_k A[g][t][k] 2^ea[g][t][k/128] * B[g*N+n][k] 2^eb[(g*N+n)/128][k/128]
 //
-// Persistent, warp-specialised CTA, one per SM (tile 128 x kBN x 128, kBN = 128
+// Persistent, warp-specialised CTA, one per SM, tile 128 x kBN x 128 (kBN = 128
 // or 256, see Cfg):
-//   warp 0     TMA producer: A tile (128 tokens x 128 k, 128B swizzle),
-//              B tile (128 rows x 128 k), the A scale words of the k-block
-//              (512 B, MN-major as the quantiser writes them); the B scales
-//              are one UE8M0 byte per (128-row block, k-block), expanded here
-//              into the 128-row scale-factor tile.
-//   warp 1     allocates TMEM; one lane issues 4 tcgen05.mma (K = 32 each) per
-//              k-block and, once per 4 k-blocks (one packed int32 of scales),
-//              tcgen05.cp of the scale factors into a TMEM slot; the whole warp
-//              first reorders the A scale words into the 32 x 16-byte layout
-//              that tcgen05.cp.32x128b.warpx4 expects.  A slot is rewritten
-//              only after a commit barrier shows the MMAs reading it are done.
-//   warps 2-   epilogue: tcgen05.ld a 128-row x 128-column slice of the fp32
-//              accumulator per warp group (each thread one row), release the
-//              accumulator, then bf16 stores or the fused per-128 FP8
-//              re-quantisation (one thread holds one whole 128-block).
-// TMEM: the accumulator(s) + (4 + kBN/32) scale-factor columns per stage.
+//   warp 0, lane 0   TMA producer: A tile (128 tokens x 128 k) and B tile
+//                    (kBN rows x 128 k), both with the 128-byte swizzle.
+//   warp 1, lane 0   MMA issuer: four tcgen05.mma (K = 32) per k-block from
+//                    precomputed descriptors, one commit per stage; once per 4
+//                    k-blocks (one packed int32 of scales) tcgen05.cp of a
+//                    staged scale-factor slot into TMEM.
+//   warp 2           scale-factor warp: loads the A scale words of a pack with
+//                    coalesced loads and stores them in the 32 x 16-byte order
+//                    tcgen05.cp.32x128b.warpx4 expects (TMEM column c of lane
+//                    r = row 32 c + r); expands the raw 128 x 128 UE8M0 weight
+//                    bytes into the kBN-row B tile; ring of kSfSlots slots
+//                    guarded by sf_full / sf_empty barriers (sf_empty is
+//                    committed after the last MMA reading the slot, so it also
+//                    guards the slot's TMEM columns).
+//   warps 3..        epilogue: per warp a 32-row x 128-column slice of the fp32
+//                    accumulator to registers (tcgen05.ld), release of the
+//                    accumulator, then bf16 stores or the fused per-128 FP8
+//                    re-quantisation (one thread holds one whole 128-block).
+// The producer and the MMA issuer are single-thread loops: their per-k-block
+// instruction chain is what feeds the tensor pipe.
 //
 // Scale factors and the K = 128 blocks: the hardware applies one UE8M0 scale
 // per 32 k (scale_vec::1X).  A 128-wide k-block is issued as four K = 32 MMAs
@@ -32,8 +36,6 @@
 // scaled by the same power of two.  The byte is chosen with the
 // scale-factor-id field of the instruction descriptor: the 4 blocks of a
 // packed int32 are bytes 0..3 of one TMEM column word.
-#include <cuda/std/cstdint>
-
 #include "dsv4_device.cuh"
 #include "dsv4_internal.h"
 
@@ -58,24 +60,22 @@ struct Cfg {
   static constexpr int kStages = (kBN == 128) ? 6 : 4;
   static constexpr int kAccBufs = (kBN == 128) ? 2 : 1;
   static constexpr int kEpiWarps = (kBN == 128) ? 4 : 8;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kEpiWarp0 = 3;
+  static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
   static constexpr uint32_t kBBytes = kBN * kBK;
+  static constexpr int kSfSlots = 4;
   static constexpr uint32_t kSfbBytes = kBN * 4;
-  // Scale factors are staged once per 4 k-blocks (one packed int32 covers four
-  // 128-wide blocks) into one of kSfSlots TMEM slots of (4 + kBN/32) columns.
-  static constexpr int kSfSlots = 3;
+  static constexpr uint32_t kSfSlotBytes = kSfaBytes + kSfbBytes;
   static constexpr int kSfCol0 = kAccBufs * kBN;              // after the accumulators
   static constexpr int kSfColsPerSlot = 4 + kBN / 32;         // A: 4, B: kBN/32
   static_assert(kSfCol0 + kSfSlots * kSfColsPerSlot <= kTmemCols, "TMEM budget");
   // shared memory plan (operand tiles 1024-byte aligned for the 128B swizzle)
   static constexpr uint32_t a = 0;
   static constexpr uint32_t b = a + kStages * kABytes;
-  static constexpr uint32_t sfa = b + kStages * kBBytes;
-  static constexpr uint32_t sfb = sfa + kStages * kSfaBytes;
-  static constexpr uint32_t bars = sfb + kStages * kSfbBytes;
-  // full[kStages], empty[kStages], tmem_full[kAccBufs], tmem_empty[kAccBufs], drain,
-  // sf_free[kSfSlots]
-  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 1 + kSfSlots;
+  static constexpr uint32_t sf = b + kStages * kBBytes;
+  static constexpr uint32_t bars = sf + kSfSlots * kSfSlotBytes;
+  // full/empty[kStages], tmem_full/empty[kAccBufs], sf_full/empty[kSfSlots], drain
+  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 2 * kSfSlots + 1;
   static constexpr uint32_t misc = bars + n_bars * 8;  // tmem base, abort flag
   static constexpr uint32_t total = misc + 16;
   static constexpr uint32_t smem_bytes = total + 1024;  // + alignment slack
@@ -84,8 +84,9 @@ struct Cfg {
 struct Params {
   int64_t T;
   int G, N, K;
-  int m_tiles, n_tiles, num_tiles, k_blocks;
+  int m_tiles, n_tiles, num_tiles, k_blocks, packs;
   int64_t t_al;
+  const int32_t* a_scale;  // int32 [G][packs][t_al]
   const uint8_t* b_scale;
   int b_scale_ld;          // K / 128
   __nv_bfloat16* out;      // [T][G*N] or null
@@ -118,13 +119,11 @@ __device__ __forceinline__ uint32_t b_scale_word(const Params& p, int rb, int j)
 template <int kBN, int kEpi>
 __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
-                             const __grid_constant__ CUtensorMap tm_b,
-                             const __grid_constant__ CUtensorMap tm_sfa, const Params p) {
+                             const __grid_constant__ CUtensorMap tm_b, const Params p) {
   using C = Cfg<kBN>;
   constexpr int kStages = C::kStages;
   constexpr int kAccBufs = C::kAccBufs;
   constexpr uint32_t kBBytes = C::kBBytes;
-  constexpr uint32_t kSfbBytes = C::kSfbBytes;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128B-swizzled operand tiles
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -132,11 +131,12 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::bars);
   uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* tmem_full = bars + 2 * kStages;
-  uint64_t* tmem_empty = bars + 2 * kStages + kAccBufs;
-  uint64_t* drain = bars + 2 * kStages + 2 * kAccBufs;
-  uint64_t* sf_free = drain + 1;
+  uint64_t* empty = full + kStages;
+  uint64_t* tmem_full = empty + kStages;
+  uint64_t* tmem_empty = tmem_full + kAccBufs;
+  uint64_t* sf_full = tmem_empty + kAccBufs;
+  uint64_t* sf_empty = sf_full + C::kSfSlots;
+  uint64_t* drain = sf_empty + C::kSfSlots;
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::misc + 4);
 
@@ -152,15 +152,17 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
       mbar_init(&tmem_full[a], 1);
       mbar_init(&tmem_empty[a], C::kEpiWarps);
     }
+    for (int i = 0; i < C::kSfSlots; ++i) {
+      mbar_init(&sf_full[i], 1);
+      mbar_init(&sf_empty[i], 1);
+    }
     mbar_init(drain, 1);
-    for (int i = 0; i < C::kSfSlots; ++i) mbar_init(&sf_free[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
-    tma_prefetch_desc(&tm_sfa);
   }
   if (warp == 1) {
     tmem_alloc(tmem_base_slot, kTmemCols);
@@ -172,17 +174,96 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
   const uint32_t tmem_base = *tmem_base_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    int stage = 0;
-    uint32_t phase = 0;
-    bool issued[kStages];
-    uint32_t issued_parity[kStages];
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;  // bit s: stage s loaded / parity of its phase
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        int g, n_blk, m_blk;
+        tile_coords(p, tile, g, n_blk, m_blk);
+        const int m0 = m_blk * kBM;
+        const int brow = g * p.N + n_blk * kBN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
+          tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBK, m0, g);
+          tma_load_2d(smem + C::b + stage * kBBytes, &tm_b, &full[stage], kb * kBK, brow);
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // drain: let every copy issued here land before the CTA exits
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) mbar_wait_drain(&full[s], (issued_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issue
+      const uint64_t adesc0 = smem_desc(smem_addr(smem + C::a), 16, 1024, 2);
+      const uint64_t bdesc0 = smem_desc(smem_addr(smem + C::b), 16, 1024, 2);
+      const uint64_t sfdesc0 = smem_desc(smem_addr(smem + C::sf), 0, 128, 0);
+      uint32_t idesc[4];
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) { issued[s] = false; issued_parity[s] = 0; }
-    const int packs = (p.k_blocks + 3) / 4;
-    bool ok = true;
-    // weight-scale words of the first tile, loaded ahead (lane j holds packs j, j+32, ...)
+      for (int i = 0; i < 4; ++i) idesc[i] = mxf8_idesc(kBM, kBN, i, i);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      uint32_t packs_done = 0;  // scale-factor packs consumed so far (all tiles)
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        uint32_t sf_col = 0;
+        int slot = 0;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          if ((kb & 3) == 0) {
+            slot = static_cast<int>(packs_done % C::kSfSlots);
+            const uint32_t sp = (packs_done / C::kSfSlots) & 1u;
+            ++packs_done;
+            if (!mbar_wait(&sf_full[slot], sp, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            sf_col = tmem_base + static_cast<uint32_t>(C::kSfCol0 + slot * C::kSfColsPerSlot);
+            const uint64_t sd = sfdesc0 + ((slot * C::kSfSlotBytes) >> 4);
+            tmem_cp_32x128b_x4(sf_col, sd);                     // A: the slot's first 512 B
+#pragma unroll
+            for (int r = 0; r < kBN / 128; ++r)                 // B: 512 B per 128 rows
+              tmem_cp_32x128b_x4(sf_col + 4 + 4 * r, sd + ((kSfaBytes + 512u * r) >> 4));
+          }
+          const uint64_t ad = adesc0 + ((stage * kABytes) >> 4);
+          const uint64_t bd = bdesc0 + ((stage * kBBytes) >> 4);
+          const uint32_t id = idesc[kb & 3];
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k)   // +32 bytes along K = +2 in the address field
+            mma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, id, sf_col, sf_col + 4,
+                     (kb | k) != 0 ? 1u : 0u);
+          mma_commit(&empty[stage]);
+          // the last k-block that reads this scale-factor slot releases it
+          if ((kb & 3) == 3 || kb == p.k_blocks - 1) mma_commit(&sf_empty[slot]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&tmem_full[acc]);
+        if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (*abort_flag) {
+        // let every MMA / copy this thread issued finish before TMEM is freed
+        mma_commit(drain);
+        mbar_wait_drain(drain, 0);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------ scale factors
     constexpr int kRb = kBN / 128;   // 128-row weight-scale blocks per tile
+    const int packs = p.packs;
     uint32_t wnext[kRb][4];
 #pragma unroll
     for (int r = 0; r < kRb; ++r)
@@ -198,6 +279,8 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
         for (int i = 0; i < 4; ++i)
           if (lane + 32 * i < packs) wnext[r][i] = b_scale_word(p, rb + r, lane + 32 * i);
     }
+    uint32_t n = 0;  // packs staged so far (all tiles)
+    bool ok = true;
     for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
       int g, n_blk, m_blk;
       tile_coords(p, tile, g, n_blk, m_blk);
@@ -217,118 +300,37 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
           for (int i = 0; i < 4; ++i)
             wnext[r][i] = (lane + 32 * i < packs) ? b_scale_word(p, rb2 + r, lane + 32 * i) : 0u;
       }
-      const int m0 = m_blk * kBM;
-      const int brow = g * p.N + n_blk * kBN;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
-        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        // scale factors only at the first k-block of each packed int32 (4 k-blocks)
-        const int j = kb >> 2;
-        const bool pack_start = (kb & 3) == 0;
-        if (pack_start) {
-          // B scale-factor tile: each 128-row block's rows share its byte
-          uint4* sfb = reinterpret_cast<uint4*>(smem + C::sfb + stage * kSfbBytes);
+      const int64_t m0 = static_cast<int64_t>(m_blk) * kBM;
+      for (int j = 0; j < packs; ++j) {
+        // the 128 scale words of this pack: lane r takes rows r, r+32, r+64, r+96
+        const int32_t* src = p.a_scale + (static_cast<int64_t>(g) * packs + j) * p.t_al + m0;
+        uint32_t v[4];
 #pragma unroll
-          for (int r = 0; r < kRb; ++r) {
-            const uint32_t src = (j < 32) ? wcur[r][0] : (j < 64) ? wcur[r][1]
+        for (int c = 0; c < 4; ++c) {
+          const int64_t t = m0 + 32 * c + lane;
+          v[c] = t < p.T ? static_cast<uint32_t>(__ldg(src + 32 * c + lane)) : 0u;
+        }
+        const int slot = static_cast<int>(n % C::kSfSlots);
+        const uint32_t sp = (n / C::kSfSlots) & 1u;
+        ++n;
+        if (!mbar_wait_warp(&sf_empty[slot], sp ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        uint4* dst = reinterpret_cast<uint4*>(smem + C::sf + slot * C::kSfSlotBytes);
+        dst[lane] = make_uint4(v[0], v[1], v[2], v[3]);
+#pragma unroll
+        for (int r = 0; r < kRb; ++r) {
+          const uint32_t src_w = (j < 32) ? wcur[r][0] : (j < 64) ? wcur[r][1]
                                : (j < 96) ? wcur[r][2] : wcur[r][3];
-            const uint32_t word = __shfl_sync(0xFFFFFFFFu, src, j & 31);
-            sfb[32 * r + lane] = make_uint4(word, word, word, word);
-          }
-          fence_proxy_async_smem();
+          const uint32_t word = __shfl_sync(0xFFFFFFFFu, src_w, j & 31);
+          dst[32 + 32 * r + lane] = make_uint4(word, word, word, word);
         }
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes + (pack_start ? kSfaBytes : 0u));
-          tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBK, m0, g);
-          tma_load_2d(smem + C::b + stage * kBBytes, &tm_b, &full[stage], kb * kBK, brow);
-          if (pack_start)
-            tma_load_3d(smem + C::sfa + stage * kSfaBytes, &tm_sfa, &full[stage], m0, j, g);
-        }
-        issued[stage] = true;
-        issued_parity[stage] = phase;
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (lane == 0) mbar_arrive(&sf_full[slot]);
       }
-    }
-    if (!ok && lane == 0) {
-      // drain: let every copy this warp issued land before the CTA exits
-      for (int s = 0; s < kStages; ++s)
-        if (issued[s]) mbar_wait_drain(&full[s], issued_parity[s]);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issue
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    uint32_t packs_done = 0;  // scale-factor packs staged so far (all tiles)
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-      if (!mbar_wait_warp(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-      uint32_t sf_col = 0;
-      int slot = 0;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
-        if (!mbar_wait_warp(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
-        if ((kb & 3) == 0) {
-          // a new pack of scale factors: wait until the MMAs that read this
-          // slot three packs ago have completed, then stage it
-          slot = static_cast<int>(packs_done % C::kSfSlots);
-          const uint32_t slot_phase = (packs_done / C::kSfSlots) & 1u;
-          if (!mbar_wait_warp(&sf_free[slot], slot_phase ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          ++packs_done;
-          // reorder the 128 A scale words: row m = 32 i + r goes to word 4 r + i
-          uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + C::sfa + stage * kSfaBytes);
-          uint32_t v0 = sfa[lane], v1 = sfa[32 + lane], v2 = sfa[64 + lane], v3 = sfa[96 + lane];
-          __syncwarp();
-          reinterpret_cast<uint4*>(sfa)[lane] = make_uint4(v0, v1, v2, v3);
-          fence_proxy_async_smem();
-          __syncwarp();
-          sf_col = tmem_base + static_cast<uint32_t>(C::kSfCol0 + slot * C::kSfColsPerSlot);
-          if (lane == 0) {
-            const uint32_t sfa_addr = smem_addr(sfa);
-            const uint32_t sfb_addr = smem_addr(smem + C::sfb + stage * kSfbBytes);
-            tmem_cp_32x128b_x4(sf_col, smem_desc(sfa_addr, 0, 128, 0));
-#pragma unroll
-            for (int r = 0; r < kBN / 128; ++r)
-              tmem_cp_32x128b_x4(sf_col + 4 + 4 * r, smem_desc(sfb_addr + 512 * r, 0, 128, 0));
-          }
-        }
-        if (lane == 0) {
-          const uint32_t a_addr = smem_addr(smem + C::a + stage * kABytes);
-          const uint32_t b_addr = smem_addr(smem + C::b + stage * kBBytes);
-          const uint32_t id = static_cast<uint32_t>(kb & 3);
-          const uint32_t idesc = mxf8_idesc(kBM, kBN, id, id);
-#pragma unroll
-          for (int k = 0; k < kBK / 32; ++k) {
-            const uint64_t ad = smem_desc(a_addr + 32u * k, 16, 1024, 2);
-            const uint64_t bd = smem_desc(b_addr + 32u * k, 16, 1024, 2);
-            mma_mxf8(d_tmem, ad, bd, idesc, sf_col, sf_col + 4, (kb | k) != 0 ? 1u : 0u);
-          }
-          mma_commit(&empty[stage]);
-          // last k-block that reads this scale-factor slot: release it on completion
-          if ((kb & 3) == 3 || kb == p.k_blocks - 1) mma_commit(&sf_free[slot]);
-        }
-        __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
-      }
-      if (!ok) break;
-      if (lane == 0) mma_commit(&tmem_full[acc]);
-      __syncwarp();
-      if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
-    }
-    if (*abort_flag && lane == 0) {
-      // let every MMA / copy this thread issued finish before TMEM is freed
-      mma_commit(drain);
-      mbar_wait_drain(drain, 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int epi = warp - 2;             // 0 .. kEpiWarps-1
+    const int epi = warp - C::kEpiWarp0;  // 0 .. kEpiWarps-1
     const int quarter = warp & 3;         // TMEM lanes this warp may access
     const int col_half = epi >> 2;        // which 128 columns of the tile
     const int row = quarter * 32 + lane;
@@ -429,6 +431,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
@@ -480,7 +483,7 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   const int64_t t_al = (T + 3) / 4 * 4;
   const int packs = (q.K / 128 + 3) / 4;
 
-  CUtensorMap tm_a, tm_b, tm_sfa;
+  CUtensorMap tm_a, tm_b;
   {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(q.K), static_cast<cuuint64_t>(T),
                           static_cast<cuuint64_t>(q.G)};
@@ -499,17 +502,6 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
                 CU_TENSOR_MAP_SWIZZLE_128B))
       return DSV4_ERR_CUDA;
   }
-  {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(packs),
-                          static_cast<cuuint64_t>(q.G)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(t_al * 4),
-                             static_cast<cuuint64_t>(t_al * 4 * packs)};
-    cuuint32_t box[3] = {kBM, 1, 1};
-    if (!encode(&tm_sfa, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, q.a_scale, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
-      return DSV4_ERR_CUDA;
-  }
-
   Params p;
   p.T = T;
   p.G = q.G;
@@ -519,7 +511,9 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   p.n_tiles = q.N / kBN;
   p.num_tiles = p.m_tiles * p.n_tiles * q.G;
   p.k_blocks = q.K / kBK;
+  p.packs = packs;
   p.t_al = t_al;
+  p.a_scale = q.a_scale;
   p.b_scale = q.b_scale;
   p.b_scale_ld = q.K / 128;
   p.out = static_cast<__nv_bfloat16*>(q.out_bf16);
@@ -529,7 +523,7 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
 
   const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
   block_scaled_gemm_kernel<kBN, kEpi>
-      <<<grid, C::kThreads, C::smem_bytes, stream>>>(tm_a, tm_b, tm_sfa, p);
+      <<<grid, C::kThreads, C::smem_bytes, stream>>>(tm_a, tm_b, p);
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
