@@ -25,8 +25,10 @@
 //                    guards the slot's TMEM columns).
 //   warps 3..        epilogue: per warp a 32-row x 128-column slice of the fp32
 //                    accumulator to registers (tcgen05.ld), release of the
-//                    accumulator, then bf16 stores or the fused per-128 FP8
-//                    re-quantisation (one thread holds one whole 128-block).
+//                    accumulator, then bf16 conversion or the fused per-128
+//                    FP8 re-quantisation (one thread holds one whole 128-block);
+//                    the results leave through a swizzled shared-memory box
+//                    and a TMA store (coalesced, rows beyond T clipped).
 // The producer and the MMA issuer are single-thread loops: their per-k-block
 // instruction chain is what feeds the tensor pipe.
 //
@@ -73,7 +75,10 @@ struct Cfg {
   static constexpr uint32_t a = 0;
   static constexpr uint32_t b = a + kStages * kABytes;
   static constexpr uint32_t sf = b + kStages * kBBytes;
-  static constexpr uint32_t bars = sf + kSfSlots * kSfSlotBytes;
+  // per epilogue warp, a 2 KiB staging buffer for its TMA stores (32 rows x 64 B)
+  static constexpr uint32_t kEpiBufBytes = 2048;
+  static constexpr uint32_t epi = (sf + kSfSlots * kSfSlotBytes + 1023) / 1024 * 1024;
+  static constexpr uint32_t bars = epi + kEpiWarps * kEpiBufBytes;
   // full/empty[kStages], tmem_full/empty[kAccBufs], sf_full/empty[kSfSlots], drain
   static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 2 * kSfSlots + 1;
   static constexpr uint32_t misc = bars + n_bars * 8;  // tmem base, abort flag
@@ -119,7 +124,8 @@ __device__ __forceinline__ uint32_t b_scale_word(const Params& p, int rb, int j)
 template <int kBN, int kEpi>
 __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
-                             const __grid_constant__ CUtensorMap tm_b, const Params p) {
+                             const __grid_constant__ CUtensorMap tm_b,
+                             const __grid_constant__ CUtensorMap tm_out, const Params p) {
   using C = Cfg<kBN>;
   constexpr int kStages = C::kStages;
   constexpr int kAccBufs = C::kAccBufs;
@@ -163,6 +169,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&tm_out);
   }
   if (warp == 1) {
     tmem_alloc(tmem_base_slot, kTmemCols);
@@ -356,22 +363,42 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      // Stores go through this warp's staging buffer: each lane writes its row's
+      // 64-byte chunk with the 64-byte TMA swizzle (16-byte unit q of row r at
+      // q ^ ((r >> 1) & 3): conflict-free), then one lane stores the 32-row box
+      // with TMA, which also clips rows beyond T.
+      uint8_t* buf = smem + C::epi + epi * C::kEpiBufBytes;
+      const int32_t box_y = static_cast<int32_t>(static_cast<int64_t>(m_blk) * kBM + quarter * 32);
+      auto stage_chunk = [&](const uint4 (&v)[4], int32_t box_x) {
+        if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(buf + 64 * lane + 16 * (q ^ ((lane >> 1) & 3))) = v[q];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && box_y < p.T) {   // a box wholly past the last row is skipped
+          tma_store_2d(&tm_out, buf, box_x, box_y);
+          bulk_commit_group();
+        }
+      };
       if constexpr (kEpi == kEpiBf16) {
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + t * ld + col0);
+        // four chunks of 32 columns (64 bytes of bf16 per row)
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          uint4 v[4];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t w[4];
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(
-                    __uint_as_float(r[c][8 * v + 2 * i]), __uint_as_float(r[c][8 * v + 2 * i + 1]));
-                w[i] = *reinterpret_cast<const uint32_t*>(&h);
-              }
-              dst[4 * c + v] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int i = 0; i < 4; ++i) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(
+                  __uint_as_float(r[c][8 * q + 2 * i]), __uint_as_float(r[c][8 * q + 2 * i + 1]));
+              w[i] = *reinterpret_cast<const uint32_t*>(&h);
             }
+            v[q] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          stage_chunk(v, static_cast<int32_t>(col0 + 32 * c));
         }
       } else {
         // z is a bf16 tensor: round first, then quantise the rounded values
@@ -384,41 +411,30 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
             r[c][i] = __float_as_uint(zr);
             amax = fmaxf(amax, fabsf(zr));
           }
+        const int e = ue8m0_exponent(amax);
+        const float inv = exp2_neg(e);
+        // two chunks of 64 columns (64 bytes of e4m3 per row)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint4 v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int c = 2 * h + (q >> 1);
+              const int b = 16 * (q & 1) + 4 * i;
+              w[i] = static_cast<uint32_t>(e4m3x2(__uint_as_float(r[c][b]) * inv,
+                                                  __uint_as_float(r[c][b + 1]) * inv)) |
+                     (static_cast<uint32_t>(e4m3x2(__uint_as_float(r[c][b + 2]) * inv,
+                                                   __uint_as_float(r[c][b + 3]) * inv))
+                      << 16);
+            }
+            v[q] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          stage_chunk(v, static_cast<int32_t>(col0 + 64 * h));
+        }
         if (live) {
-          if (p.out != nullptr) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint4* dst = reinterpret_cast<uint4*>(p.out + t * ld + col0 + 32 * c);
-#pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                uint32_t w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  w[i] = (r[c][8 * v + 2 * i] >> 16) | (r[c][8 * v + 2 * i + 1] & 0xFFFF0000u);
-                dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
-          }
-          const int e = ue8m0_exponent(amax);
-          const float inv = exp2_neg(e);
-          uint4* qdst = reinterpret_cast<uint4*>(p.q_out + t * ld + col0);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
-              uint32_t w[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int b = 16 * v + 4 * i;
-                w[i] = static_cast<uint32_t>(e4m3x2(__uint_as_float(r[c][b]) * inv,
-                                                    __uint_as_float(r[c][b + 1]) * inv)) |
-                       (static_cast<uint32_t>(e4m3x2(__uint_as_float(r[c][b + 2]) * inv,
-                                                     __uint_as_float(r[c][b + 3]) * inv))
-                        << 16);
-              }
-              qdst[2 * c + v] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
           const int64_t blk = col0 / 128;  // 128-column block of the flattened row
           uint8_t* sbytes = reinterpret_cast<uint8_t*>(p.q_scale);
           sbytes[((blk >> 2) * p.t_al + t) * 4 + (blk & 3)] = static_cast<uint8_t>(e + 127);
@@ -426,6 +442,8 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
       }
       if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_all();   // every store complete before the CTA leaves
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -502,6 +520,18 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
                 CU_TENSOR_MAP_SWIZZLE_128B))
       return DSV4_ERR_CUDA;
   }
+  CUtensorMap tm_out;
+  {
+    const int64_t ld = static_cast<int64_t>(q.G) * q.N;
+    const bool quant = kEpi == kEpiQuant;
+    const void* base = quant ? static_cast<const void*>(q.q_out) : q.out_bf16;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(ld), static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * (quant ? 1 : 2))};
+    cuuint32_t box[2] = {quant ? 64u : 32u, 32u};   // 64-byte rows
+    if (!encode(&tm_out, quant ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+      return DSV4_ERR_CUDA;
+  }
   Params p;
   p.T = T;
   p.G = q.G;
@@ -523,7 +553,7 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
 
   const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
   block_scaled_gemm_kernel<kBN, kEpi>
-      <<<grid, C::kThreads, C::smem_bytes, stream>>>(tm_a, tm_b, p);
+      <<<grid, C::kThreads, C::smem_bytes, stream>>>(tm_a, tm_b, tm_out, p);
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 

@@ -33,7 +33,7 @@ struct GemmProblem {
   const void* b = nullptr;          // e4m3 [G*N][K] row-major
   const uint8_t* b_scale = nullptr; // UE8M0 bytes [G*N/128][K/128]
   int epilogue = kEpiBf16;
-  void* out_bf16 = nullptr;         // bf16 [T][G*N] (required for kEpiBf16, optional for kEpiQuant)
+  void* out_bf16 = nullptr;         // bf16 [T][G*N] (kEpiBf16)
   uint8_t* q_out = nullptr;         // e4m3 [T][G*N]           (kEpiQuant)
   int32_t* q_scale = nullptr;       // int32 [ceil(G*N/512)][T_al] (kEpiQuant)
 };
