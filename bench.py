@@ -46,6 +46,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--workload", default="full",
+                    choices=["full", "tiny", "decode", "prefill", "quant1k", "quant8k", "quant32k"],
+                    help="full: the O-projection (default); decode / prefill: quant + grouped "
+                         "wo_a; quantNk: the quantiser alone (timed by CUDA-graph replay over "
+                         "rotating input sets)")
     return ap.parse_args()
 
 
@@ -346,11 +351,136 @@ def run_reference(args, ws, rank):
     }
 
 
+# ------------------------------------------------- per-workload reports --
+def _graph_ms(fn, steps: int, stream) -> float:
+    """Device time of `steps` calls of fn, captured in CUDA graphs and replayed
+    (no host launch overhead in the measurement)."""
+    chunk = min(steps, 100)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(chunk):
+            fn(i)
+    reps = max(1, steps // chunk)
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * chunk)
+
+
+def run_workload(args, ws, rank, local):
+    """One of the smaller synthetic workloads: quant (+ grouped wo_a).  Each step
+    uses the next of several rotating input sets whose total exceeds 3x L2, so
+    that weights and activations come from HBM, not from the previous step."""
+    import deepseek_v4_attention_gb300 as k
+
+    if ws > 1:
+        raise SystemExit("--workload other than full runs on one GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = di.WORKLOADS[args.workload]
+    gemm = not w.name.startswith("quant")
+    host = di.make_inputs(w, with_wo_b=False)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = host["o"].numel() * 2 + (host["wo_a"].numel() if gemm else 0) + \
+        w.n_groups * w.T * w.D + (w.T * w.n_groups * w.o_lora_rank * 2 if gemm else 0)
+    nsets = max(1, min(32, -(-3 * l2 // set_bytes)))
+    T_al = k.tma_aligned_tokens(w.T)
+    sets = []
+    for i in range(nsets):
+        st = {n: host[n].to(dev) for n in ("o", "positions", "cache")}
+        st["x"] = torch.empty(w.n_groups, w.T, w.D, dtype=torch.float8_e4m3fn, device=dev)
+        st["xs"] = torch.empty(w.n_groups, (w.D // 128 + 3) // 4, T_al, dtype=torch.int32,
+                               device=dev)
+        if gemm:
+            st["wo_a"] = host["wo_a"].to(dev)
+            st["wo_a_scale"] = host["wo_a_scale"].to(dev)
+            st["z"] = torch.empty(w.T, w.n_groups, w.o_lora_rank, dtype=torch.bfloat16,
+                                  device=dev)
+        sets.append(st)
+    stream = torch.cuda.Stream(dev)
+
+    def quant(i):
+        st = sets[i % nsets]
+        return k.dsv4_inv_rope_fp8_quant(st["o"], st["positions"], st["cache"], w.n_groups,
+                                         w.heads_per_group, out_fp8=st["x"], out_scale=st["xs"],
+                                         stream=stream)
+
+    def wo_a(i):
+        st = sets[i % nsets]
+        k.dsv4_grouped_wo_a(st["x"].transpose(0, 1), st["xs"].permute(2, 0, 1)[:w.T],
+                            st["wo_a"], st["wo_a_scale"], w.n_groups, w.o_lora_rank, z=st["z"],
+                            stream=stream)
+
+    def step(i):
+        quant(i)
+        if gemm:
+            wo_a(i)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize()
+    launches_per_step = 2 if gemm else 1
+    with ClockSampler(local) as clk:
+        ms_step = _graph_ms(step, args.steps, stream)
+        ms_q = _graph_ms(quant, args.steps, stream)
+        ms_a = _graph_ms(wo_a, args.steps, stream) if gemm else 0.0
+    if k.dsv4_device_status(clear=True) != 0:
+        raise RuntimeError("device status error")
+    peaks, src = measured_peaks()
+    qbytes = w.T * w.H * (1024 + 512 + 4) + w.T * (8 + 256)
+    stages = {"quant": {"ms": ms_q, "bound": "hbm", "algorithmic": qbytes,
+                        "achieved": qbytes / (ms_q * 1e-3) / 1e9, "unit": "GB/s",
+                        "peak": peaks["hbm_gbs"]}}
+    if gemm:
+        fl = 2.0 * w.T * w.n_groups * w.o_lora_rank * w.D
+        by = w.n_groups * w.o_lora_rank * w.D + w.n_groups * w.T * w.D + \
+            w.T * w.n_groups * w.o_lora_rank * 2
+        if w.name == "decode":      # weight-read bound: bytes against HBM
+            stages["wo_a"] = {"ms": ms_a, "bound": "hbm", "algorithmic": by,
+                              "achieved": by / (ms_a * 1e-3) / 1e9, "unit": "GB/s",
+                              "peak": peaks["hbm_gbs"]}
+        else:
+            stages["wo_a"] = {"ms": ms_a, "bound": "tensor", "algorithmic": fl,
+                              "achieved": fl / (ms_a * 1e-3) / 1e12, "unit": "TFLOP/s",
+                              "peak": 2.0 * peaks.get("bf16_tflops_sustained",
+                                                      peaks["bf16_tflops"])}
+    for s_ in stages.values():
+        s_["frac"] = s_["achieved"] / s_["peak"]
+    dom = max(stages, key=lambda n: stages[n]["ms"])
+    ds = stages[dom]
+    result = {
+        "metric": METRIC, "value": w.T / (ms_step * 1e-3), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded; random FP8 block-scaled weights)",
+        "config": {"workload": f"{w.name}: T={w.T}, {w.H} heads x 512 ({w.n_groups} groups x "
+                               f"{w.heads_per_group})" + (f", o_lora_rank {w.o_lora_rank}, "
+                               "quant + grouped wo_a" if gemm else ", quantiser alone"),
+                   "timing": "CUDA-graph replay", "input_sets": nsets,
+                   "l2": f"{nsets} rotating input sets of {set_bytes / 1e6:.1f} MB (>= 3x L2)"},
+        "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
+                     "peak": ds["peak"], "unit": ds["unit"], "frac": ds["frac"],
+                     "traffic": None, "peak_source": src},
+        "stages": stages,
+    }
+    return result
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, ws, rank)
+    elif args.workload != "full":
+        res = run_workload(args, ws, rank, local)
     else:
         res = run_ours(args, ws, rank, local)
     if rank == 0 and res is not None:

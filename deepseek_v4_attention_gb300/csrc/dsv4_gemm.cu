@@ -121,7 +121,7 @@ __device__ __forceinline__ uint32_t b_scale_word(const Params& p, int rb, int j)
   return w;
 }
 
-template <int kBN, int kEpi>
+template <int kBN, int kEpi, int kSplit>
 __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b,
@@ -148,6 +148,16 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+
+  // Split-K (kSplit > 1): a cluster of kSplit CTAs shares one output tile, CTA
+  // r of the cluster taking k-blocks [r, r+1) * k_blocks / kSplit; otherwise a
+  // persistent loop over tiles.
+  const int split_rank = (kSplit > 1) ? static_cast<int>(cluster_cta_rank()) : 0;
+  const int tile0 = (kSplit > 1) ? static_cast<int>(blockIdx.x) / kSplit
+                                 : static_cast<int>(blockIdx.x);
+  const int tile_step = (kSplit > 1) ? p.num_tiles : static_cast<int>(gridDim.x);
+  const int kb0 = split_rank * (p.k_blocks / kSplit);
+  const int kb1 = kb0 + p.k_blocks / kSplit;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -187,12 +197,12 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // bit s: stage s loaded / parity of its phase
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
         int g, n_blk, m_blk;
         tile_coords(p, tile, g, n_blk, m_blk);
         const int m0 = m_blk * kBM;
         const int brow = g * p.N + n_blk * kBN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
           tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBK, m0, g);
@@ -223,13 +233,13 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
       uint32_t acc_phase = 0;
       uint32_t packs_done = 0;  // scale-factor packs consumed so far (all tiles)
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
         if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
         uint32_t sf_col = 0;
         int slot = 0;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           if ((kb & 3) == 0) {
@@ -251,10 +261,10 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBK / 32; ++k)   // +32 bytes along K = +2 in the address field
             mma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, id, sf_col, sf_col + 4,
-                     (kb | k) != 0 ? 1u : 0u);
+                     ((kb - kb0) | k) != 0 ? 1u : 0u);
           mma_commit(&empty[stage]);
           // the last k-block that reads this scale-factor slot releases it
-          if ((kb & 3) == 3 || kb == p.k_blocks - 1) mma_commit(&sf_empty[slot]);
+          if ((kb & 3) == 3 || kb == kb1 - 1) mma_commit(&sf_empty[slot]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -276,9 +286,9 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
     for (int r = 0; r < kRb; ++r)
 #pragma unroll
       for (int i = 0; i < 4; ++i) wnext[r][i] = 0u;
-    if (blockIdx.x < p.num_tiles) {
+    if (tile0 < p.num_tiles) {
       int g, nb, mb;
-      tile_coords(p, blockIdx.x, g, nb, mb);
+      tile_coords(p, tile0, g, nb, mb);
       const int rb = (g * p.N + nb * kBN) / 128;
 #pragma unroll
       for (int r = 0; r < kRb; ++r)
@@ -288,7 +298,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
     }
     uint32_t n = 0;  // packs staged so far (all tiles)
     bool ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+    for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
       int g, n_blk, m_blk;
       tile_coords(p, tile, g, n_blk, m_blk);
       uint32_t wcur[kRb][4];
@@ -296,7 +306,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
       for (int r = 0; r < kRb; ++r)
 #pragma unroll
         for (int i = 0; i < 4; ++i) wcur[r][i] = wnext[r][i];
-      const int next = tile + gridDim.x;
+      const int next = tile + tile_step;
       if (next < p.num_tiles) {
         int g2, nb2, mb2;
         tile_coords(p, next, g2, nb2, mb2);
@@ -308,7 +318,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
             wnext[r][i] = (lane + 32 * i < packs) ? b_scale_word(p, rb2 + r, lane + 32 * i) : 0u;
       }
       const int64_t m0 = static_cast<int64_t>(m_blk) * kBM;
-      for (int j = 0; j < packs; ++j) {
+      for (int j = kb0 / 4; j < (kb1 + 3) / 4; ++j) {
         // the 128 scale words of this pack: lane r takes rows r, r+32, r+64, r+96
         const int32_t* src = p.a_scale + (static_cast<int64_t>(g) * packs + j) * p.t_al + m0;
         uint32_t v[4];
@@ -344,7 +354,8 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
     const int64_t ld = static_cast<int64_t>(p.G) * p.N;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    bool synced = false;  // split-K: this warp took part in the two cluster barriers
+    for (int tile = tile0; tile < p.num_tiles; tile += tile_step) {
       int g, n_blk, m_blk;
       tile_coords(p, tile, g, n_blk, m_blk);
       if (!mbar_wait_warp(&tmem_full[acc], acc_phase, abort_flag, p.status)) break;
@@ -363,6 +374,41 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      if constexpr (kSplit > 1) {
+        // Split-K: the other CTAs of the cluster add their partial tiles into
+        // this one.  Every pipeline of the cluster has drained by the first
+        // barrier, so the leader's A stage buffers are free; each warp slice
+        // (32 rows x 128 fp32) has its own 16 KiB there, laid out [col/4][lane].
+        cluster_sync();
+        const uint32_t part = smem_addr(smem + C::a) + static_cast<uint32_t>(epi) * 16384u;
+        if (split_rank != 0) {
+          const uint32_t dst = map_to_cta(part, 0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              st_cluster_v4(dst + static_cast<uint32_t>(((c * 8 + v) * 32 + lane) * 16),
+                            r[c][4 * v], r[c][4 * v + 1], r[c][4 * v + 2], r[c][4 * v + 3]);
+        }
+        cluster_sync();
+        synced = true;
+        if (split_rank == 0) {
+          for (int peer = 1; peer < kSplit; ++peer) {
+            const float4* src = reinterpret_cast<const float4*>(smem + C::a + epi * 16384);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const float4 q = src[(c * 8 + v) * 32 + lane];
+                r[c][4 * v] = __float_as_uint(__uint_as_float(r[c][4 * v]) + q.x);
+                r[c][4 * v + 1] = __float_as_uint(__uint_as_float(r[c][4 * v + 1]) + q.y);
+                r[c][4 * v + 2] = __float_as_uint(__uint_as_float(r[c][4 * v + 2]) + q.z);
+                r[c][4 * v + 3] = __float_as_uint(__uint_as_float(r[c][4 * v + 3]) + q.w);
+              }
+          }
+        }
+      }
+      if (split_rank == 0) {
       // Stores go through this warp's staging buffer: each lane writes its row's
       // 64-byte chunk with the 64-byte TMA swizzle (16-byte unit q of row r at
       // q ^ ((r >> 1) & 3): conflict-free), then one lane stores the 32-row box
@@ -440,10 +486,22 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
           sbytes[((blk >> 2) * p.t_al + t) * 4 + (blk & 3)] = static_cast<uint8_t>(e + 127);
         }
       }
+      }  // split_rank == 0
       if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
     }
     if (lane == 0) bulk_wait_all();   // every store complete before the CTA leaves
     __syncwarp();
+    if (kSplit > 1 && !synced) {       // aborted before the reduction: still meet the cluster
+      cluster_sync();
+      cluster_sync();
+    }
+  }
+  if constexpr (kSplit > 1) {
+    if (warp < C::kEpiWarp0) {         // producer, MMA and scale-factor warps
+      __syncwarp();                    // lane 0 of warps 0 and 1 finished its loop
+      cluster_sync();
+      cluster_sync();
+    }
   }
 
   tc_fence_before();
@@ -485,13 +543,13 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kBN, int kEpi>
+template <int kBN, int kEpi, int kSplit>
 int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
   using C = Cfg<kBN>;
   static int configured_for[64] = {0};
   if (dev.device < 0 || dev.device >= 64) return DSV4_ERR_UNSUPPORTED;
   if (!configured_for[dev.device]) {
-    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi>,
+    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi, kSplit>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::smem_bytes)) != cudaSuccess)
       return DSV4_ERR_CUDA;
@@ -551,9 +609,28 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   p.q_scale = q.q_scale;
   p.status = dev.status;
 
-  const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
-  block_scaled_gemm_kernel<kBN, kEpi>
-      <<<grid, C::kThreads, C::smem_bytes, stream>>>(tm_a, tm_b, tm_out, p);
+  if (kSplit == 1) {
+    const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
+    block_scaled_gemm_kernel<kBN, kEpi, 1>
+        <<<grid, C::kThreads, C::smem_bytes, stream>>>(tm_a, tm_b, tm_out, p);
+    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+  }
+  // one cluster of kSplit CTAs per output tile
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles * kSplit));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kSplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_kernel<kBN, kEpi, kSplit>, tm_a, tm_b, tm_out,
+                         p) != cudaSuccess)
+    return DSV4_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
@@ -566,11 +643,19 @@ int launch_block_scaled_gemm(const GemmProblem& q, cudaStream_t stream, const De
   const int64_t m_tiles = (q.T + kBM - 1) / kBM;
   const bool wide = q.N % 256 == 0 && m_tiles * (q.N / 256) * q.G >= dev.num_sms;
   if (wide) {
-    if (q.epilogue == kEpiQuant) return launch_impl<256, kEpiQuant>(q, stream, dev);
-    return launch_impl<256, kEpiBf16>(q, stream, dev);
+    if (q.epilogue == kEpiQuant) return launch_impl<256, kEpiQuant, 1>(q, stream, dev);
+    return launch_impl<256, kEpiBf16, 1>(q, stream, dev);
   }
-  if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant>(q, stream, dev);
-  return launch_impl<128, kEpiBf16>(q, stream, dev);
+  // Too few 128-wide tiles to fill the GPU (decode): split K over a 2-CTA
+  // cluster when both halves hold whole scale packs (k_blocks % 8 == 0).
+  const int64_t tiles = m_tiles * (q.N / 128) * q.G;
+  const bool split = (q.K / 128) % 8 == 0 && 2 * tiles <= dev.num_sms;
+  if (split) {
+    if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 2>(q, stream, dev);
+    return launch_impl<128, kEpiBf16, 2>(q, stream, dev);
+  }
+  if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 1>(q, stream, dev);
+  return launch_impl<128, kEpiBf16, 1>(q, stream, dev);
 }
 
 }  // namespace dsv4
