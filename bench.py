@@ -361,14 +361,15 @@ def _graph_ms(fn, steps: int, stream) -> float:
         for i in range(chunk):
             fn(i)
     reps = max(1, steps // chunk)
-    g.replay()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
+    with torch.cuda.stream(stream):          # replay on the stream the events are on
         g.replay()
-    e1.record(stream)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / (reps * chunk)
 
