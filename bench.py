@@ -68,6 +68,28 @@ def workload(args) -> di.Workload:
     return w
 
 
+def rank_workload(w: di.Workload, rank: int) -> di.Workload:
+    """Token shard of one rank: the same shapes and weights, its own T tokens."""
+    import dataclasses
+    return dataclasses.replace(w, seed=w.seed + 1000 * rank,
+                               weight_seed=w.seed if w.weight_seed is None else w.weight_seed)
+
+
+def reduce_max(x: float, device) -> float:
+    """Max of a per-rank scalar over all ranks (the slowest rank's time)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, steps: int, ms_total: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world * steps / (ms_total / 1e3)
+
+
 def config_of(w: di.Workload, n_gpus: int) -> dict:
     return {
         "workload": f"full O-projection: T={w.T} tokens/GPU, {w.H} heads x 512 "
@@ -147,8 +169,7 @@ def run_ours(args, ws, rank, local):
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    w = workload(args)
-    w = w.with_tokens(w.T, seed=w.seed + 1000 * rank)       # each rank its own tokens
+    w = rank_workload(workload(args), rank)                 # each rank its own tokens
     host = di.make_inputs(w)
     d = {n: t.to(dev) for n, t in host.items()}
     need = k.dsv4_o_proj_workspace_bytes(w.T, w.n_groups, w.heads_per_group, w.head_dim,
@@ -167,12 +188,7 @@ def run_ours(args, ws, rank, local):
             dist.barrier()
 
     def max_over_ranks(x: float) -> float:
-        if ws == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dev)
 
     # per-kernel events, recorded by the library between its three launches
     n_ev = args.steps
@@ -203,7 +219,7 @@ def run_ours(args, ws, rank, local):
     if k.dsv4_device_status(clear=True) != 0:
         raise RuntimeError("device status error in the timed region")
     ms_step = ms_total / args.steps
-    value = w.T * ws * args.steps / (ms_total / 1e3)
+    value = job_throughput(w.T, ws, args.steps, ms_total)
 
     stage_ms = [0.0, 0.0, 0.0]
     for e in evs:

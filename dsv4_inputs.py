@@ -51,6 +51,7 @@ class Workload:
     nope_dim: int = 448
     rope_dim: int = 64
     quant_group_size: int = 128
+    weight_seed: int | None = None  # None: derived from `seed`
 
     @property
     def head_dim(self) -> int:
@@ -156,10 +157,11 @@ def make_inputs(w: Workload, with_wo_b: bool = True) -> dict:
         "positions": positions(w),
         "cache": cos_sin_cache(w.max_pos, w.rope_dim),
     }
-    d["wo_a"], d["wo_a_scale"] = fp8_block_weight(w.n_groups * w.o_lora_rank, w.D, w.seed + 101)
+    ws = w.seed if w.weight_seed is None else w.weight_seed
+    d["wo_a"], d["wo_a_scale"] = fp8_block_weight(w.n_groups * w.o_lora_rank, w.D, ws + 101)
     if with_wo_b:
         d["wo_b"], d["wo_b_scale"] = fp8_block_weight(w.hidden, w.n_groups * w.o_lora_rank,
-                                                      w.seed + 202)
+                                                      ws + 202)
     return d
 
 
