@@ -152,6 +152,29 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def recorded_traffic(kernel: str) -> float | None:
+    """DRAM bytes per launch of `kernel` from the committed ncu summary of the
+    full workload, or None when the kernel sources changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic_full_T4096.txt")
+    if not os.path.exists(path):
+        return None
+    csrc = os.path.join(ROOT, "deepseek_v4_attention_gb300", "csrc")
+    vals = []
+    with open(path) as f:
+        for line in f:
+            tok = line.split()
+            if not tok or tok[0].startswith("#"):
+                continue
+            if tok[0] == "source":
+                with open(os.path.join(csrc, tok[1]), "rb") as g:
+                    if hashlib.sha256(g.read()).hexdigest() != tok[2]:
+                        return None
+            elif tok[0] == kernel:
+                vals.append(float(tok[1]) + float(tok[2]))
+    return sum(vals) / len(vals) if vals else None
+
+
 def measured_peaks() -> tuple[dict, str]:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -283,7 +306,7 @@ def run_ours(args, ws, rank, local):
     ds = stages[dom]
     roofline = {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
                 "peak": ds["peak"], "unit": ds["unit"], "frac": ds["frac"],
-                "traffic": None,
+                "traffic": recorded_traffic(dom) if w.T == 4096 else None,
                 "peak_source": f"{src}: " + ("fp8 = 2 x bf16_tflops_sustained"
                                               if ds["bound"] == "tensor" else "hbm_gbs")}
 
