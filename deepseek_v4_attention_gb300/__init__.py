@@ -69,6 +69,8 @@ def load_library() -> ctypes.CDLL:
     lib.dsv4_status_string.restype = ctypes.c_char_p
     lib.dsv4_device_status.argtypes = [P, I]
     lib.dsv4_device_status.restype = I
+    lib.dsv4_selftest_wait_timeout.argtypes = [I64, P]
+    lib.dsv4_selftest_wait_timeout.restype = I
     lib.dsv4_last_launch_count.argtypes = []
     lib.dsv4_last_launch_count.restype = I
     _lib = lib
@@ -268,6 +270,12 @@ def dsv4_o_proj_static(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: 
 def dsv4_device_status(clear: bool = True, stream=None) -> int:
     """Device status word (0 = OK, else a negative dsv4_status); synchronises the stream."""
     return int(load_library().dsv4_device_status(_stream(stream), 1 if clear else 0))
+
+
+def dsv4_selftest_wait_timeout(limit_us: int = 1000, stream=None) -> None:
+    """Runs the bounded-wait self-test kernel (see include/dsv4.h)."""
+    _check(load_library().dsv4_selftest_wait_timeout(limit_us, _stream(stream)),
+           "dsv4_selftest_wait_timeout")
 
 
 def dsv4_status_string(status: int) -> str:

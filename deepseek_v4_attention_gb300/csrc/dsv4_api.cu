@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "../../include/dsv4.h"
+#include "dsv4_device.cuh"
 #include "dsv4_internal.h"
 
 namespace dsv4 {
@@ -15,6 +16,24 @@ namespace dsv4 {
 __device__ int g_status_word = 0;
 
 namespace {
+
+// Diagnostics: one thread waits, with the pipelines' bounded wait, on an
+// mbarrier that nothing ever arrives on.  The wait gives up after limit_ns,
+// records DSV4_ERR_TIMEOUT and the kernel returns normally.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    (void)mbar_wait(&bar, 0, &abort_flag, status, limit_ns);  // phase 0 never completes
+  }
+  __syncthreads();
+}
 
 constexpr int kMaxDevices = 64;
 DeviceInfo g_devices[kMaxDevices];
@@ -283,6 +302,16 @@ int dsv4_o_proj_with_events(const void* o, const int64_t* positions, const float
   if (!mark(3)) return DSV4_ERR_CUDA;
   t_last_launches = 3;
   return DSV4_OK;
+}
+
+int dsv4_selftest_wait_timeout(int64_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return DSV4_ERR_SHAPE;
+  DeviceInfo dev;
+  int rc = get_device_info(&dev);
+  if (rc != DSV4_OK) return rc;
+  wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint64_t>(limit_us) * 1000u, dev.status);
+  return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
 int dsv4_device_status(void* stream, int clear) {

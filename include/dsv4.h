@@ -221,6 +221,18 @@ const char* dsv4_status_string(int status);
  */
 int dsv4_device_status(void* stream, int clear);
 
+/*
+ * Diagnostics for the failure path of the kernels' pipeline waits (the pages
+ * have no counterpart).  Enqueues one small kernel whose single waiting thread
+ * uses the same bounded wait as the GEMM pipelines on a barrier that nothing
+ * ever arrives on, with a limit of limit_us microseconds (1 .. 1,000,000)
+ * instead of the pipelines' 2 s.  The wait gives up, records DSV4_ERR_TIMEOUT
+ * in the device status word and the kernel returns normally: no trap, no
+ * fault, the context stays usable.  Read the result with dsv4_device_status().
+ * DSV4_ERR_SHAPE for a limit out of range.
+ */
+int dsv4_selftest_wait_timeout(int64_t limit_us, void* stream);
+
 /* Number of kernel launches the last successful compute call on this host
  * thread enqueued (0 for T == 0).  For accounting in benchmarks. */
 int dsv4_last_launch_count(void);

@@ -20,7 +20,7 @@ def test_exports_every_header_function(lib):
     names = k.header_functions()
     assert set(names) == {"dsv4_inv_rope_fp8_quant", "dsv4_grouped_wo_a",
                           "dsv4_o_proj_workspace_bytes", "dsv4_o_proj", "dsv4_o_proj_with_events",
-                          "dsv4_o_proj_static",
+                          "dsv4_o_proj_static", "dsv4_selftest_wait_timeout",
                           "dsv4_status_string",
                           "dsv4_device_status", "dsv4_last_launch_count"}
     out = subprocess.run(["nm", "-D", "--defined-only", k.LIB_PATH], capture_output=True,
@@ -116,3 +116,8 @@ def test_o_proj_static_host_validation_without_gpu(lib):
     assert f(*a) == -5
     a = list(good); a[16] = None
     assert f(*a) == -2
+
+
+def test_selftest_limit_validation_without_gpu(lib):
+    assert lib.dsv4_selftest_wait_timeout(0, None) == -1
+    assert lib.dsv4_selftest_wait_timeout(2_000_000, None) == -1

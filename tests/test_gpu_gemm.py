@@ -184,3 +184,30 @@ def test_o_proj_errors(dev):
     assert lib.dsv4_o_proj(*bad) == 0 and k.dsv4_last_launch_count() == 0
     torch.cuda.synchronize()
     assert k.dsv4_device_status(clear=True) == 0
+
+
+def test_grouped_wo_a_on_prequantized_rope_quant_layout(dev):
+    """A QuantizedActivation in the RopeQuant layout (o_proj page,
+    rope_quant_attn_out: 16 group slots of 8 heads x 512, physical [group,
+    token, K], scales [group, 8, T_al]) with only the first n_groups live: the
+    padding groups are sliced off (deep_gemm_fp8_o_proj) and go straight into
+    the grouped GEMM.  Padding slots hold NaN codes and garbage scales, which
+    must not reach z."""
+    import deepseek_v4_attention_gb300 as k
+    T, slots, D, R, live = 48, 16, 4096, 1024, 12
+    T_al = k.tma_aligned_tokens(T)
+    x, xs = di.random_fp8_activation(T, live, D, seed=77, tma_aligned_T=T_al)
+    data = torch.full((slots, T, D), 0x7F, dtype=torch.uint8)        # NaN codes everywhere
+    data[:live] = x
+    scale = torch.full((slots, D // 512, T_al), 0x7F7F7F7F, dtype=torch.int32)
+    scale[:live] = xs
+    w, ws = di.fp8_block_weight(live * R, D, seed=78)
+    view = data.to(dev).view(torch.float8_e4m3fn).transpose(0, 1)    # [T, 16, 4096]
+    sview = scale.to(dev).permute(2, 0, 1)[:T]                        # [T, 16, 8]
+    z = k.dsv4_grouped_wo_a(view[:, :live], sview[:, :live], w.to(dev), ws.to(dev), live, R)
+    torch.cuda.synchronize()
+    assert k.dsv4_device_status(clear=True) == 0
+    _, z64 = oracle.grouped_gemm(x, xs, w, ws, T, live, D, R, want_fp64=True)
+    zg = to_bits(z)
+    assert not np.isnan(torch.from_numpy(zg.view(np.int16)).view(torch.bfloat16).float().numpy()).any()
+    assert gemm_rel_err(zg, z64) <= GEMM_RTOL

@@ -150,3 +150,15 @@ def test_quant_out_of_range_position_sets_status(dev):
                               w.heads_per_group)
     assert k.dsv4_device_status(clear=True) == k._NAME_TO_CODE["DSV4_ERR_RANGE"]
     assert k.dsv4_device_status(clear=True) == 0
+
+
+def test_pipeline_wait_timeout_is_reported_not_trapped(dev):
+    """The bounded wait of the GEMM pipelines, run on a barrier nothing arrives
+    on with a 2 ms limit: the kernel returns, the host reads DSV4_ERR_TIMEOUT,
+    and the device keeps working (a quantisation right after is still exact)."""
+    import deepseek_v4_attention_gb300 as k
+    k.dsv4_device_status(clear=True)
+    k.dsv4_selftest_wait_timeout(2000)
+    assert k.dsv4_device_status(clear=True) == k._NAME_TO_CODE["DSV4_ERR_TIMEOUT"]
+    assert k.dsv4_device_status(clear=True) == 0
+    _compare(di.WORKLOADS["tiny"], dev)
