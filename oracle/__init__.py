@@ -66,6 +66,8 @@ def _load():
             "oracle_grouped_gemm": (ctypes.c_int, [P, P, I64, I64, I64, I64, P, P, P, P]),
             "oracle_o_proj": (ctypes.c_int, [P, P, P, I64, I64, I64, I64, I64, I64, I64, I64, I64,
                                              P, P, P, P, P, P, P]),
+            "oracle_inv_rope_bf16": (ctypes.c_int, [P, P, P, I64, I64, I64, I64, I64, I64, P]),
+            "oracle_grouped_gemm_bf16": (ctypes.c_int, [P, P, I64, I64, I64, I64, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -244,3 +246,32 @@ def o_proj(o, positions, cache, wo_a, wo_a_scale, wo_b, wo_b_scale, *, n_groups:
                                _ptr(z), _ptr(out64), _ptr(out))
     _check(rc, "o_proj")
     return out, out64, z
+
+
+def inv_rope_bf16(o, positions, cache, n_groups: int, heads_per_group: int,
+                  nope_dim: int = 448, rope_dim: int = 64, max_pos: int | None = None):
+    """quantize=False: bf16 bits, physical [G, T, D]."""
+    o = _np(o, np.uint16)
+    T = o.shape[0]
+    positions = _np(positions, np.int64)
+    cache = _np(cache, np.float32)
+    if max_pos is None:
+        max_pos = cache.shape[0]
+    D = heads_per_group * (nope_dim + rope_dim)
+    out = np.zeros((n_groups, T, D), dtype=np.uint16)
+    _check(_load().oracle_inv_rope_bf16(_ptr(o), _ptr(positions), _ptr(cache), T, max_pos,
+                                        n_groups, heads_per_group, nope_dim, rope_dim,
+                                        _ptr(out)), "inv_rope_bf16")
+    return out
+
+
+def grouped_gemm_bf16(x_bf16, w_bf16, T: int, G: int, D: int, R: int, want_fp64: bool = False):
+    """bf16 grouped product: x physical [G, T, D], w [G*R, D] -> bf16 bits [T, G, R]."""
+    x = _np(x_bf16, np.uint16)
+    w = _np(w_bf16, np.uint16)
+    assert x.size == G * T * D and w.size == G * R * D
+    z = np.empty((T, G, R), dtype=np.uint16)
+    z64 = np.empty((T, G, R), dtype=np.float64) if want_fp64 else None
+    _check(_load().oracle_grouped_gemm_bf16(_ptr(x), _ptr(w), T, G, D, R, _ptr(z64), _ptr(z)),
+           "grouped_gemm_bf16")
+    return (z, z64) if want_fp64 else z

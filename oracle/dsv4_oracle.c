@@ -335,6 +335,77 @@ int oracle_inv_rope_fp8_quant(const uint16_t* o, const int64_t* positions, const
     return OR_OK;
 }
 
+/*
+ * The quantize=False variant ([grouped_wo_a] grouped_input: "The BF16
+ * inverse-rotated groups, [num_tokens, n_groups, group_dim]"; [o_proj]
+ * deep_gemm_fp8_o_proj passes quantize=use_fp8): steps 1-2 of O-1, then every
+ * value rounded to bf16 (nearest, ties to even).  Nope lanes come back exactly.
+ * out_bf16 physical [G][T][D], the same group-major layout as the FP8 codes.
+ */
+int oracle_inv_rope_bf16(const uint16_t* o, const int64_t* positions, const float* cache,
+                         int64_t T, int64_t max_pos, int64_t n_groups, int64_t heads_per_group,
+                         int64_t nope_dim, int64_t rope_dim, uint16_t* out_bf16)
+{
+    const int64_t head_dim = nope_dim + rope_dim;
+    const int64_t H = n_groups * heads_per_group;
+    if (n_groups <= 0 || heads_per_group <= 0 || nope_dim < 0 || rope_dim <= 0 || rope_dim % 2)
+        return OR_ERR_SHAPE;
+    if (T < 0 || max_pos <= 0) return OR_ERR_SHAPE;
+    if (T == 0) return OR_OK;
+    if (!o || !positions || !cache || !out_bf16) return OR_ERR_NULL;
+    for (int64_t t = 0; t < T; t++)
+        if (positions[t] < 0 || positions[t] >= max_pos) return OR_ERR_RANGE;
+    const int64_t D = heads_per_group * head_dim;
+    const int64_t half = rope_dim / 2;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; t++) {
+        const float* crow = cache + positions[t] * rope_dim;
+        for (int64_t h = 0; h < H; h++) {
+            const int64_t g = h / heads_per_group, hh = h % heads_per_group;
+            const uint16_t* src = o + (t * H + h) * head_dim;
+            uint16_t* dst = out_bf16 + (g * T + t) * D + hh * head_dim;
+            for (int64_t j = 0; j < nope_dim; j++) dst[j] = src[j];
+            for (int64_t i = 0; i < half; i++) {
+                float y0, y1;
+                oracle_inv_rope_pair(oracle_bf16_to_float(src[nope_dim + 2 * i]),
+                                     oracle_bf16_to_float(src[nope_dim + 2 * i + 1]), crow[i],
+                                     crow[half + i], &y0, &y1);
+                dst[nope_dim + 2 * i] = oracle_bf16_from_double((double)y0);
+                dst[nope_dim + 2 * i + 1] = oracle_bf16_from_double((double)y1);
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/*
+ * The bf16 grouped product ([o_proj] deep_gemm_fp8_o_proj when wo_a is not
+ * FP8: torch.bmm of the [G, T, D] groups with wo_a.weight viewed [G, R, D],
+ * transposed):  z[t, g, n] = sum_k x[g][t][k] * W[g*R + n][k], fp64 sum,
+ * bf16 result.   x_bf16 physical [G][T][D], w_bf16 [G*R][D], z [T][G][R].
+ */
+int oracle_grouped_gemm_bf16(const uint16_t* x_bf16, const uint16_t* w_bf16, int64_t T, int64_t G,
+                             int64_t D, int64_t R, double* z64, uint16_t* z_bf16)
+{
+    if (T < 0 || G <= 0 || D <= 0 || R <= 0) return OR_ERR_SHAPE;
+    if (T == 0) return OR_OK;
+    if (!x_bf16 || !w_bf16 || !z_bf16) return OR_ERR_NULL;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t tg = 0; tg < T * G; tg++) {
+        const int64_t t = tg / G, g = tg % G;
+        const uint16_t* xr = x_bf16 + (g * T + t) * D;
+        for (int64_t n = 0; n < R; n++) {
+            const uint16_t* wr = w_bf16 + (g * R + n) * D;
+            double acc = 0.0;
+            for (int64_t k = 0; k < D; k++)
+                acc += (double)oracle_bf16_to_float(xr[k]) * (double)oracle_bf16_to_float(wr[k]);
+            if (z64) z64[(t * G + g) * R + n] = acc;
+            z_bf16[(t * G + g) * R + n] = oracle_bf16_from_double(acc);
+        }
+    }
+    return OR_OK;
+}
+
 /* The same steps without rotation, on a plain [T, C] bf16 matrix: the per-token
  * 1 x qgs block quantisation that the FP8 wo_b projection applies to the
  * flattened bf16 z ([o_proj] deep_gemm_fp8_o_proj returns wo_b(z.flatten(1));

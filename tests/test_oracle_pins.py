@@ -463,3 +463,45 @@ def test_o_proj_chain_on_tiny(oracle_mod):
     wd = _dequant_torch(d["wo_b"], ew)
     ref = (zd @ wd.T).numpy()
     assert np.allclose(out64, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+
+# ---------------------------------------------------------------------------
+# bf16 variants (quantize=False, and the bmm fallback for a non-FP8 wo_a)
+# ---------------------------------------------------------------------------
+
+def test_inv_rope_bf16_closed_form_and_identity(oracle_mod):
+    w = di.WORKLOADS["tiny"]
+    d = di.make_inputs(w, with_wo_b=False)
+    xb = oracle_mod.inv_rope_bf16(d["o"], d["positions"], d["cache"], w.n_groups,
+                                  w.heads_per_group)
+    got = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).double().numpy()
+    y = _bruteforce_quant(d["o"], d["positions"], d["cache"], w.n_groups, w.heads_per_group)
+    y = y.reshape(w.T, w.n_groups, w.D).transpose(1, 0, 2)          # physical [G, T, D]
+    # nope lanes exact; rotated lanes within half a bf16 step (+ fp32 slack) of fp64
+    lanes = np.arange(w.D) % 512
+    nope = lanes < 448
+    assert np.array_equal(got[:, :, nope], y[:, :, nope])
+    r = got[:, :, ~nope] - y[:, :, ~nope]
+    step = np.exp2(np.floor(np.log2(np.maximum(np.abs(y[:, :, ~nope]), 1e-30))) - 7)
+    assert np.all(np.abs(r) <= step / 2 + 4 * f32_ulp(y[:, :, ~nope]))
+    # position 0: bit-identical to o, group-major
+    p0 = torch.zeros(w.T, dtype=torch.int64)
+    x0 = oracle_mod.inv_rope_bf16(d["o"], p0, d["cache"], w.n_groups, w.heads_per_group)
+    ref = d["o"].view(torch.uint16).reshape(w.T, w.n_groups, w.D).permute(1, 0, 2).numpy()
+    assert np.array_equal(x0, ref)
+
+
+def test_grouped_gemm_bf16_matches_bmm_in_float64(oracle_mod):
+    """The page's own restatement: torch.bmm of x [G, T, D] with W viewed [G, R, D]
+    transposed, here in float64."""
+    T, G, D, R = 7, 3, 192, 64
+    rng = np.random.default_rng(9)
+    x = torch.from_numpy(rng.standard_normal((G, T, D)).astype(np.float32)).to(torch.bfloat16)
+    wt = torch.from_numpy(rng.standard_normal((G * R, D)).astype(np.float32) * 0.02).to(torch.bfloat16)
+    z, z64 = oracle_mod.grouped_gemm_bf16(x, wt, T, G, D, R, want_fp64=True)
+    ref = torch.bmm(x.double(), wt.double().view(G, R, D).transpose(1, 2)).transpose(0, 1).numpy()
+    assert np.allclose(z64, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    zb = torch.from_numpy(z.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(zb, torch.from_numpy(ref).to(torch.bfloat16).double().numpy()) or \
+        np.max(np.abs(zb - ref) / np.maximum(np.abs(ref), 1e-30)) <= 2 ** -8
