@@ -69,6 +69,10 @@ def load_library() -> ctypes.CDLL:
     lib.dsv4_status_string.restype = ctypes.c_char_p
     lib.dsv4_device_status.argtypes = [P, I]
     lib.dsv4_device_status.restype = I
+    lib.dsv4_inv_rope_bf16.argtypes = [P, P, P, I64, I64, I, I, I, I, P, P]
+    lib.dsv4_inv_rope_bf16.restype = I
+    lib.dsv4_grouped_wo_a_bf16.argtypes = [P, I64, I, I, I, P, P, P]
+    lib.dsv4_grouped_wo_a_bf16.restype = I
     lib.dsv4_selftest_wait_timeout.argtypes = [I64, P]
     lib.dsv4_selftest_wait_timeout.restype = I
     lib.dsv4_last_launch_count.argtypes = []
@@ -175,6 +179,52 @@ def dsv4_grouped_wo_a(x_fp8: torch.Tensor, x_scale: torch.Tensor, w_fp8: torch.T
     rc = lib.dsv4_grouped_wo_a(x_fp8.data_ptr(), x_scale.data_ptr(), T, G, D, o_lora_rank,
                                w_fp8.data_ptr(), w_scale.data_ptr(), z.data_ptr(), _stream(stream))
     _check(rc, "dsv4_grouped_wo_a")
+    return z
+
+
+def dsv4_inv_rope_bf16(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                       n_groups: int, heads_per_group: int, nope_dim: int = 448,
+                       rope_dim: int = 64, *, out: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """quantize=False: returns the bf16 inverse-rotated groups [T, G, D] with
+    strides (D, T*D, 1)."""
+    lib = load_library()
+    _cuda(o, "o", torch.bfloat16)
+    _cuda(positions, "positions", torch.int64)
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    if o.dim() != 3 or not o.is_contiguous():
+        raise ValueError("o must be a contiguous [T, H, head_dim] tensor")
+    T, H, hd = o.shape
+    if H != n_groups * heads_per_group or hd != nope_dim + rope_dim or positions.numel() != T:
+        raise DSV4Error(-1, "dsv4_inv_rope_bf16 (shapes)")
+    D = heads_per_group * hd
+    if out is None:
+        out = torch.empty((n_groups, T, D), dtype=torch.bfloat16, device=o.device)
+    rc = lib.dsv4_inv_rope_bf16(o.data_ptr(), positions.data_ptr(), cos_sin_cache.data_ptr(), T,
+                                cos_sin_cache.shape[0], n_groups, heads_per_group, nope_dim,
+                                rope_dim, out.data_ptr(), _stream(stream))
+    _check(rc, "dsv4_inv_rope_bf16")
+    return out.transpose(0, 1)
+
+
+def dsv4_grouped_wo_a_bf16(x_bf16: torch.Tensor, w_bf16: torch.Tensor, n_groups: int,
+                           o_lora_rank: int, *, z: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """bf16 grouped product (bmm path): x [T, G, D] view of a physical [G, T, D]
+    buffer, w [G*R, D]; returns bf16 z [T, G, R]."""
+    lib = load_library()
+    _cuda(x_bf16, "x_bf16", torch.bfloat16)
+    _cuda(w_bf16, "w_bf16", torch.bfloat16)
+    T, G, D = x_bf16.shape
+    if G != n_groups or x_bf16.stride() != (D, T * D, 1):
+        raise ValueError("x_bf16 must be the [T, G, D] view of a physical [G, T, D] buffer")
+    if tuple(w_bf16.shape) != (G * o_lora_rank, D) or not w_bf16.is_contiguous():
+        raise ValueError("w_bf16 must be a contiguous [G*R, D] tensor")
+    if z is None:
+        z = torch.empty((T, G, o_lora_rank), dtype=torch.bfloat16, device=x_bf16.device)
+    rc = lib.dsv4_grouped_wo_a_bf16(x_bf16.data_ptr(), T, G, D, o_lora_rank, w_bf16.data_ptr(),
+                                    z.data_ptr(), _stream(stream))
+    _check(rc, "dsv4_grouped_wo_a_bf16")
     return z
 
 

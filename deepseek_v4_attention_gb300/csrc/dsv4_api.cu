@@ -184,6 +184,54 @@ int dsv4_grouped_wo_a(const void* x_fp8, const int32_t* x_scale, int64_t num_tok
   return rc;
 }
 
+int dsv4_inv_rope_bf16(const void* o, const int64_t* positions, const float* cos_sin_cache,
+                       int64_t num_tokens, int64_t max_pos, int n_groups, int heads_per_group,
+                       int nope_dim, int rope_dim, void* out_bf16, void* stream) {
+  t_last_launches = 0;
+  int rc = check_quant_shapes(num_tokens, max_pos, n_groups, heads_per_group, nope_dim, rope_dim,
+                              128);
+  if (rc != DSV4_OK) return rc;
+  if ((rc = check_quant_supported(nope_dim, rope_dim, 128)) != DSV4_OK) return rc;
+  if (num_tokens == 0) return DSV4_OK;
+  if (!o || !positions || !cos_sin_cache || !out_bf16) return DSV4_ERR_NULL;
+  if (!aligned16(o) || !aligned16(positions) || !aligned16(cos_sin_cache) || !aligned16(out_bf16))
+    return DSV4_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = get_device_info(&dev)) != DSV4_OK) return rc;
+  rc = launch_inv_rope_bf16(o, positions, cos_sin_cache, num_tokens, max_pos, n_groups,
+                            heads_per_group, out_bf16, static_cast<cudaStream_t>(stream), dev);
+  if (rc == DSV4_OK) t_last_launches = 1;
+  return rc;
+}
+
+int dsv4_grouped_wo_a_bf16(const void* x_bf16, int64_t num_tokens, int n_groups, int group_dim,
+                           int o_lora_rank, const void* w_bf16, void* z, void* stream) {
+  t_last_launches = 0;
+  if (num_tokens < 0 || n_groups <= 0 || group_dim <= 0 || o_lora_rank <= 0 ||
+      group_dim % 64 != 0 || o_lora_rank % 128 != 0)
+    return DSV4_ERR_SHAPE;
+  if (num_tokens == 0) return DSV4_OK;
+  if (!x_bf16 || !w_bf16 || !z) return DSV4_ERR_NULL;
+  if (!aligned16(x_bf16) || !aligned16(w_bf16) || !aligned16(z)) return DSV4_ERR_ALIGN;
+  if (num_tokens > (int64_t(1) << 31) - 128) return DSV4_ERR_SHAPE;
+  DeviceInfo dev;
+  int rc = get_device_info(&dev);
+  if (rc != DSV4_OK) return rc;
+  GemmProblem p;
+  p.T = num_tokens;
+  p.G = n_groups;
+  p.N = o_lora_rank;
+  p.K = group_dim;
+  p.a = x_bf16;
+  p.b = w_bf16;
+  p.bf16 = true;
+  p.epilogue = kEpiBf16;
+  p.out_bf16 = z;
+  rc = launch_block_scaled_gemm(p, static_cast<cudaStream_t>(stream), dev);
+  if (rc == DSV4_OK) t_last_launches = 1;
+  return rc;
+}
+
 size_t dsv4_o_proj_workspace_bytes(int64_t num_tokens, int n_groups, int heads_per_group,
                                    int head_dim, int o_lora_rank) {
   if (num_tokens < 0 || n_groups <= 0 || heads_per_group <= 0 || head_dim <= 0 ||

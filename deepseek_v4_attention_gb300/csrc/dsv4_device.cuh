@@ -258,6 +258,29 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulate,
+// both K-major: [4,6) D format (F32 = 1), [7,10) A format (BF16 = 1),
+// [10,13) B format (BF16 = 1), [17,23) N >> 3, [24,29) M >> 4.
+__device__ __forceinline__ uint32_t bf16_idesc(uint32_t M, uint32_t N) {
+  uint32_t d = 0;
+  d |= 1u << 4;
+  d |= 1u << 7;
+  d |= 1u << 10;
+  d |= ((N >> 3) & 0x3Fu) << 17;
+  d |= ((M >> 4) & 0x1Fu) << 24;
+  return d;
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives on an mbarrier once every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {

@@ -121,7 +121,7 @@ __device__ __forceinline__ uint32_t b_scale_word(const Params& p, int rb, int j)
   return w;
 }
 
-template <int kBN, int kEpi, int kSplit>
+template <int kBN, int kEpi, int kSplit, bool kBf16>
 __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b,
@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
   constexpr int kStages = C::kStages;
   constexpr int kAccBufs = C::kAccBufs;
   constexpr uint32_t kBBytes = C::kBBytes;
+  // elements of K per k-block: 128 e4m3 or 64 bf16 (128 bytes, one swizzle row)
+  constexpr int kBKe = kBf16 ? 64 : kBK;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128B-swizzled operand tiles
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -205,8 +207,8 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
-          tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBK, m0, g);
-          tma_load_2d(smem + C::b + stage * kBBytes, &tm_b, &full[stage], kb * kBK, brow);
+          tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBKe, m0, g);
+          tma_load_2d(smem + C::b + stage * kBBytes, &tm_b, &full[stage], kb * kBKe, brow);
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
       const uint64_t sfdesc0 = smem_desc(smem_addr(smem + C::sf), 0, 128, 0);
       uint32_t idesc[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) idesc[i] = mxf8_idesc(kBM, kBN, i, i);
+      for (int i = 0; i < 4; ++i) idesc[i] = kBf16 ? bf16_idesc(kBM, kBN) : mxf8_idesc(kBM, kBN, i, i);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -242,7 +244,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          if ((kb & 3) == 0) {
+          if (!kBf16 && (kb & 3) == 0) {
             slot = static_cast<int>(packs_done % C::kSfSlots);
             const uint32_t sp = (packs_done / C::kSfSlots) & 1u;
             ++packs_done;
@@ -258,13 +260,19 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
           const uint64_t ad = adesc0 + ((stage * kABytes) >> 4);
           const uint64_t bd = bdesc0 + ((stage * kBBytes) >> 4);
           const uint32_t id = idesc[kb & 3];
+          // four MMAs per k-block: K = 32 e4m3 or K = 16 bf16, 32 bytes each
+          // (+32 bytes along K = +2 in the descriptor's address field)
 #pragma unroll
-          for (int k = 0; k < kBK / 32; ++k)   // +32 bytes along K = +2 in the address field
-            mma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, id, sf_col, sf_col + 4,
-                     ((kb - kb0) | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {
+            if constexpr (kBf16)
+              mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, id, ((kb - kb0) | k) != 0 ? 1u : 0u);
+            else
+              mma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, id, sf_col, sf_col + 4,
+                       ((kb - kb0) | k) != 0 ? 1u : 0u);
+          }
           mma_commit(&empty[stage]);
           // the last k-block that reads this scale-factor slot releases it
-          if ((kb & 3) == 3 || kb == kb1 - 1) mma_commit(&sf_empty[slot]);
+          if (!kBf16 && ((kb & 3) == 3 || kb == kb1 - 1)) mma_commit(&sf_empty[slot]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -277,7 +285,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
         mbar_wait_drain(drain, 0);
       }
     }
-  } else if (warp == 2) {
+  } else if (warp == 2 && !kBf16) {
     // ------------------------------------------------------ scale factors
     constexpr int kRb = kBN / 128;   // 128-row weight-scale blocks per tile
     const int packs = p.packs;
@@ -345,13 +353,12 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
         if (lane == 0) mbar_arrive(&sf_full[slot]);
       }
     }
-  } else {
+  } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
     const int epi = warp - C::kEpiWarp0;  // 0 .. kEpiWarps-1
     const int quarter = warp & 3;         // TMEM lanes this warp may access
     const int col_half = epi >> 2;        // which 128 columns of the tile
     const int row = quarter * 32 + lane;
-    const int64_t ld = static_cast<int64_t>(p.G) * p.N;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool synced = false;  // split-K: this warp took part in the two cluster barriers
@@ -543,13 +550,13 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kBN, int kEpi, int kSplit>
+template <int kBN, int kEpi, int kSplit, bool kBf16>
 int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
   using C = Cfg<kBN>;
   static int configured_for[64] = {0};
   if (dev.device < 0 || dev.device >= 64) return DSV4_ERR_UNSUPPORTED;
   if (!configured_for[dev.device]) {
-    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi, kSplit>,
+    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::smem_bytes)) != cudaSuccess)
       return DSV4_ERR_CUDA;
@@ -559,23 +566,27 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   const int64_t t_al = (T + 3) / 4 * 4;
   const int packs = (q.K / 128 + 3) / 4;
 
+  // operands: 128-byte rows of K (128 e4m3 or 64 bf16 elements) per k-block
+  const int esz = kBf16 ? 2 : 1;
+  const int kbe = kBK / esz;
+  const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUtensorMap tm_a, tm_b;
   {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(q.K), static_cast<cuuint64_t>(T),
                           static_cast<cuuint64_t>(q.G)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.K), static_cast<cuuint64_t>(T * q.K)};
-    cuuint32_t box[3] = {kBK, kBM, 1};
-    if (!encode(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q.a, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_128B))
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.K) * esz,
+                             static_cast<cuuint64_t>(T * q.K) * esz};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kbe), kBM, 1};
+    if (!encode(&tm_a, dt, 3, q.a, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return DSV4_ERR_CUDA;
   }
   {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(q.K),
                           static_cast<cuuint64_t>(static_cast<int64_t>(q.G) * q.N)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(q.K)};
-    cuuint32_t box[2] = {kBK, kBN};
-    if (!encode(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q.b, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_128B))
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(q.K) * esz};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kbe), kBN};
+    if (!encode(&tm_b, dt, 2, q.b, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return DSV4_ERR_CUDA;
   }
   CUtensorMap tm_out;
@@ -598,7 +609,7 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   p.m_tiles = static_cast<int>((T + kBM - 1) / kBM);
   p.n_tiles = q.N / kBN;
   p.num_tiles = p.m_tiles * p.n_tiles * q.G;
-  p.k_blocks = q.K / kBK;
+  p.k_blocks = q.K / kbe;
   p.packs = packs;
   p.t_al = t_al;
   p.a_scale = q.a_scale;
@@ -611,7 +622,7 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
 
   if (kSplit == 1) {
     const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
-    block_scaled_gemm_kernel<kBN, kEpi, 1>
+    block_scaled_gemm_kernel<kBN, kEpi, 1, kBf16>
         <<<grid, C::kThreads, C::smem_bytes, stream>>>(tm_a, tm_b, tm_out, p);
     return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
   }
@@ -628,8 +639,8 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_kernel<kBN, kEpi, kSplit>, tm_a, tm_b, tm_out,
-                         p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16>, tm_a, tm_b,
+                         tm_out, p) != cudaSuccess)
     return DSV4_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
@@ -642,20 +653,28 @@ int launch_block_scaled_gemm(const GemmProblem& q, cudaStream_t stream, const De
   // otherwise 128-wide tiles (twice the CTAs, for the small decode shapes)
   const int64_t m_tiles = (q.T + kBM - 1) / kBM;
   const bool wide = q.N % 256 == 0 && m_tiles * (q.N / 256) * q.G >= dev.num_sms;
-  if (wide) {
-    if (q.epilogue == kEpiQuant) return launch_impl<256, kEpiQuant, 1>(q, stream, dev);
-    return launch_impl<256, kEpiBf16, 1>(q, stream, dev);
-  }
   // Too few 128-wide tiles to fill the GPU (decode): split K over a 2-CTA
-  // cluster when both halves hold whole scale packs (k_blocks % 8 == 0).
+  // cluster when both halves hold whole k-blocks (and, for FP8, whole scale
+  // packs: k_blocks % 8 == 0).
   const int64_t tiles = m_tiles * (q.N / 128) * q.G;
-  const bool split = (q.K / 128) % 8 == 0 && 2 * tiles <= dev.num_sms;
-  if (split) {
-    if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 2>(q, stream, dev);
-    return launch_impl<128, kEpiBf16, 2>(q, stream, dev);
+  const int kbs = q.bf16 ? q.K / 64 : q.K / 128;
+  const bool split = !wide && kbs % (q.bf16 ? 2 : 8) == 0 && 2 * tiles <= dev.num_sms;
+  if (q.bf16) {
+    if (q.epilogue != kEpiBf16) return DSV4_ERR_UNSUPPORTED;
+    if (wide) return launch_impl<256, kEpiBf16, 1, true>(q, stream, dev);
+    if (split) return launch_impl<128, kEpiBf16, 2, true>(q, stream, dev);
+    return launch_impl<128, kEpiBf16, 1, true>(q, stream, dev);
   }
-  if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 1>(q, stream, dev);
-  return launch_impl<128, kEpiBf16, 1>(q, stream, dev);
+  if (wide) {
+    if (q.epilogue == kEpiQuant) return launch_impl<256, kEpiQuant, 1, false>(q, stream, dev);
+    return launch_impl<256, kEpiBf16, 1, false>(q, stream, dev);
+  }
+  if (split) {
+    if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 2, false>(q, stream, dev);
+    return launch_impl<128, kEpiBf16, 2, false>(q, stream, dev);
+  }
+  if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 1, false>(q, stream, dev);
+  return launch_impl<128, kEpiBf16, 1, false>(q, stream, dev);
 }
 
 }  // namespace dsv4

@@ -28,11 +28,12 @@ struct GemmProblem {
   int G = 1;              // groups: group g of A meets rows g*N:(g+1)*N of B
   int N = 0;              // output columns per group (multiple of 128)
   int K = 0;              // reduction length (multiple of 128)
-  const void* a = nullptr;          // e4m3 physical [G][T][K]
+  const void* a = nullptr;          // e4m3 (or bf16) physical [G][T][K]
   const int32_t* a_scale = nullptr; // int32 physical [G][ceil(K/512)][T_al]
   const void* b = nullptr;          // e4m3 [G*N][K] row-major
   const uint8_t* b_scale = nullptr; // UE8M0 bytes [G*N/128][K/128]
   int epilogue = kEpiBf16;
+  bool bf16 = false;                // A and B bf16, no scales (kind::f16), K % 64 == 0
   void* out_bf16 = nullptr;         // bf16 [T][G*N] (kEpiBf16)
   uint8_t* q_out = nullptr;         // e4m3 [T][G*N]           (kEpiQuant)
   int32_t* q_scale = nullptr;       // int32 [ceil(G*N/512)][T_al] (kEpiQuant)
@@ -43,6 +44,10 @@ int get_device_info(DeviceInfo* out);
 int launch_inv_rope_fp8_quant(const void* o, const int64_t* positions, const float* cache,
                               int64_t T, int64_t max_pos, int n_groups, int hpg, void* out_fp8,
                               int32_t* out_scale, cudaStream_t stream, const DeviceInfo& dev);
+
+int launch_inv_rope_bf16(const void* o, const int64_t* positions, const float* cache, int64_t T,
+                         int64_t max_pos, int n_groups, int hpg, void* out, cudaStream_t stream,
+                         const DeviceInfo& dev);
 
 int launch_block_scaled_gemm(const GemmProblem& p, cudaStream_t stream, const DeviceInfo& dev);
 

@@ -152,6 +152,87 @@ __global__ void __launch_bounds__(256) inv_rope_fp8_quant_kernel(
   }
 }
 
+// quantize=False: the same load / rotation, bf16 out in the group-major layout.
+// Nope lanes are stored exactly as loaded; rotated lanes are rounded to bf16.
+template <int kU>
+__global__ void __launch_bounds__(256) inv_rope_bf16_kernel(
+    const uint16_t* __restrict__ o, const int64_t* __restrict__ positions,
+    const float* __restrict__ cache, int64_t T, int64_t max_pos, int H, int hpg,
+    uint16_t* __restrict__ out, int* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t groups = T * (H / kU);
+  const int64_t D = static_cast<int64_t>(hpg) * kHeadDim;
+  const bool rope_lane = lane >= 24;
+  const int quad = lane - 24;
+  for (int64_t item = warp; item < groups; item += nwarps) {
+    const int64_t t = item / (H / kU);
+    const int h0 = static_cast<int>(item - t * (H / kU)) * kU;
+    const uint4* src = reinterpret_cast<const uint4*>(o + (t * H + h0) * kHeadDim);
+    uint4 v0[kU], v1[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      v0[u] = __ldcs(src + u * (kHeadDim / 8) + lane);
+      v1[u] = __ldcs(src + u * (kHeadDim / 8) + 32 + lane);
+    }
+    float4 c = make_float4(1.f, 1.f, 1.f, 1.f), sn = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool rotate = false;
+    if (rope_lane) {
+      const int64_t pos = __ldg(positions + t);
+      if (pos >= 0 && pos < max_pos) {
+        const float4* row = reinterpret_cast<const float4*>(cache + pos * kRope);
+        c = __ldg(row + quad);
+        sn = __ldg(row + 8 + quad);
+        rotate = true;
+      } else {
+        record_status(status, DSV4_ERR_RANGE);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      uint4 w1 = v1[u];
+      if (rotate) {
+        float f1[8];
+        unpack8(v1[u], f1);
+        inv_rotate(f1[0], f1[1], c.x, sn.x);
+        inv_rotate(f1[2], f1[3], c.y, sn.y);
+        inv_rotate(f1[4], f1[5], c.z, sn.z);
+        inv_rotate(f1[6], f1[7], c.w, sn.w);
+        uint32_t wv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(f1[2 * i], f1[2 * i + 1]);
+          wv[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        w1 = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      }
+      const int h = h0 + u;
+      const int g = h / hpg;
+      const int hh = h - g * hpg;
+      uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<int64_t>(g) * T + t) * D +
+                                            static_cast<int64_t>(hh) * kHeadDim);
+      __stcs(dst + lane, v0[u]);
+      __stcs(dst + 32 + lane, w1);
+    }
+  }
+}
+
+template <int kU>
+void launch_bf16_u(const void* o, const int64_t* positions, const float* cache, int64_t T,
+                   int64_t max_pos, int H, int hpg, void* out, cudaStream_t stream,
+                   const DeviceInfo& dev) {
+  const int threads = 256;
+  const int64_t items = T * (H / kU);
+  int64_t blocks = (items * 32 + threads - 1) / threads;
+  const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * (2048 / threads);
+  if (blocks > max_blocks) blocks = max_blocks;
+  if (blocks < 1) blocks = 1;
+  inv_rope_bf16_kernel<kU><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      static_cast<const uint16_t*>(o), positions, cache, T, max_pos, H, hpg,
+      static_cast<uint16_t*>(out), dev.status);
+}
+
 template <int kU>
 void launch_u(const void* o, const int64_t* positions, const float* cache, int64_t T,
               int64_t max_pos, int H, int hpg, void* out_fp8, int32_t* out_scale,
@@ -181,6 +262,19 @@ int launch_inv_rope_fp8_quant(const void* o, const int64_t* positions, const flo
     launch_u<2>(o, positions, cache, T, max_pos, H, hpg, out_fp8, out_scale, stream, dev);
   else
     launch_u<1>(o, positions, cache, T, max_pos, H, hpg, out_fp8, out_scale, stream, dev);
+  return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+int launch_inv_rope_bf16(const void* o, const int64_t* positions, const float* cache, int64_t T,
+                         int64_t max_pos, int n_groups, int hpg, void* out, cudaStream_t stream,
+                         const DeviceInfo& dev) {
+  const int H = n_groups * hpg;
+  if (H % 4 == 0)
+    launch_bf16_u<4>(o, positions, cache, T, max_pos, H, hpg, out, stream, dev);
+  else if (H % 2 == 0)
+    launch_bf16_u<2>(o, positions, cache, T, max_pos, H, hpg, out, stream, dev);
+  else
+    launch_bf16_u<1>(o, positions, cache, T, max_pos, H, hpg, out, stream, dev);
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 

@@ -112,6 +112,39 @@ int dsv4_grouped_wo_a(const void* x_fp8, const int32_t* x_scale, int64_t num_tok
                       const uint8_t* w_scale, void* z, void* stream);
 
 /*
+ * quantize=False variant of dsv4_inv_rope_fp8_quant: the bf16 inverse-rotated
+ * groups (vLLM docs, grouped_wo_a, grouped_input: "The BF16 inverse-rotated
+ * groups, [num_tokens, n_groups, group_dim]"; o_proj page,
+ * deep_gemm_fp8_o_proj with quantize=use_fp8 false for a non-FP8 wo_a).
+ *
+ *   o, positions, cos_sin_cache, sizes: as dsv4_inv_rope_fp8_quant
+ *   out_bf16   device bf16, physical [G][T][D] (the [T, G, D] view with strides
+ *              (D, T*D, 1)); nope lanes are copied exactly, each rotated value
+ *              is the fp32 rotation rounded to bf16 (nearest, ties to even).
+ *
+ * Errors: as dsv4_inv_rope_fp8_quant (quant_group_size is not an argument).
+ */
+int dsv4_inv_rope_bf16(const void* o, const int64_t* positions, const float* cos_sin_cache,
+                       int64_t num_tokens, int64_t max_pos, int n_groups, int heads_per_group,
+                       int nope_dim, int rope_dim, void* out_bf16, void* stream);
+
+/*
+ * Grouped wo_a with bf16 operands: the o_proj page's path for a non-FP8 wo_a,
+ * torch.bmm of the [G, T, D] groups with wo_a.weight viewed [G, R, D]
+ * transposed, into a bf16 z [T, G, R]; fp32 accumulation on the tensor cores
+ * (tcgen05 kind::f16).
+ *
+ *   x_bf16   device bf16 physical [G][T][D] (out_bf16 of the call above)
+ *   w_bf16   device bf16 [G*R, D] row-major
+ *   z        device bf16 [T, G, R] contiguous
+ *
+ * Errors: DSV4_ERR_SHAPE unless D is a positive multiple of 64 and R of 128;
+ * DSV4_ERR_NULL / DSV4_ERR_ALIGN (16 bytes) for pointers.
+ */
+int dsv4_grouped_wo_a_bf16(const void* x_bf16, int64_t num_tokens, int n_groups, int group_dim,
+                           int o_lora_rank, const void* w_bf16, void* z, void* stream);
+
+/*
  * Bytes of caller-owned scratch that dsv4_o_proj needs for these sizes: the
  * quantised groups x [G][T][D] with their scales [G][PK][T_al], and the
  * per-128 re-quantised z [T][G*R] with its scales [G*R/512][T_al] (each part

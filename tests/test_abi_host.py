@@ -21,6 +21,7 @@ def test_exports_every_header_function(lib):
     assert set(names) == {"dsv4_inv_rope_fp8_quant", "dsv4_grouped_wo_a",
                           "dsv4_o_proj_workspace_bytes", "dsv4_o_proj", "dsv4_o_proj_with_events",
                           "dsv4_o_proj_static", "dsv4_selftest_wait_timeout",
+                          "dsv4_inv_rope_bf16", "dsv4_grouped_wo_a_bf16",
                           "dsv4_status_string",
                           "dsv4_device_status", "dsv4_last_launch_count"}
     out = subprocess.run(["nm", "-D", "--defined-only", k.LIB_PATH], capture_output=True,
@@ -121,3 +122,26 @@ def test_o_proj_static_host_validation_without_gpu(lib):
 def test_selftest_limit_validation_without_gpu(lib):
     assert lib.dsv4_selftest_wait_timeout(0, None) == -1
     assert lib.dsv4_selftest_wait_timeout(2_000_000, None) == -1
+
+
+def test_bf16_entries_host_validation_without_gpu(lib):
+    P = 4096
+    f = lib.dsv4_inv_rope_bf16
+    good = [P, P, P, 4, 16, 2, 2, 448, 64, P, None]
+    a = list(good); a[3] = -1
+    assert f(*a) == -1
+    a = list(good); a[3] = 0
+    assert f(*a) == 0
+    a = list(good); a[9] = None
+    assert f(*a) == -2
+    a = list(good); a[7] = 192
+    assert f(*a) == -4
+    g = lib.dsv4_grouped_wo_a_bf16
+    good = [P, 16, 2, 1024, 128, P, P, None]
+    for idx, val in [(3, 96), (4, 64), (1, -1)]:
+        a = list(good); a[idx] = val
+        assert g(*a) == -1
+    a = list(good); a[5] = None
+    assert g(*a) == -2
+    a = list(good); a[6] = P + 2
+    assert g(*a) == -3

@@ -211,3 +211,56 @@ def test_grouped_wo_a_on_prequantized_rope_quant_layout(dev):
     zg = to_bits(z)
     assert not np.isnan(torch.from_numpy(zg.view(np.int16)).view(torch.bfloat16).float().numpy()).any()
     assert gemm_rel_err(zg, z64) <= GEMM_RTOL
+
+
+
+# ---------------------------------------------------------------------------
+# bf16 variants: quantize=False and the bf16 grouped product (bmm path)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("decode", 64), ("quant1k", 129)])
+def test_inv_rope_bf16_parity(dev, name, T):
+    import deepseek_v4_attention_gb300 as k
+    w = di.WORKLOADS[name].with_tokens(T, seed=T + 3)
+    d = di.make_inputs(w, with_wo_b=False)
+    x = k.dsv4_inv_rope_bf16(d["o"].to(dev), d["positions"].to(dev), d["cache"].to(dev),
+                             w.n_groups, w.heads_per_group)
+    torch.cuda.synchronize()
+    assert k.dsv4_device_status(clear=True) == 0
+    assert x.shape == (w.T, w.n_groups, w.D) and x.stride() == (w.D, w.T * w.D, 1)
+    ref = oracle.inv_rope_bf16(d["o"], d["positions"], d["cache"], w.n_groups, w.heads_per_group)
+    got = to_bits(x.transpose(0, 1))
+    assert np.array_equal(got, ref)          # same fp32 order, same rounding: bit-exact
+
+
+@pytest.mark.parametrize("T,G,D,R", [(16, 2, 1024, 128), (64, 8, 4096, 1024), (3, 1, 64, 128),
+                                     (129, 3, 640, 384), (1200, 4, 512, 1024)])
+def test_grouped_wo_a_bf16_parity(dev, T, G, D, R):
+    import deepseek_v4_attention_gb300 as k
+    rng = np.random.default_rng(T + G)
+    x = torch.from_numpy(rng.standard_normal((G, T, D)).astype(np.float32)).to(torch.bfloat16)
+    wt = torch.from_numpy(rng.standard_normal((G * R, D)).astype(np.float32) * 0.02).to(
+        torch.bfloat16)
+    z = k.dsv4_grouped_wo_a_bf16(x.to(dev).transpose(0, 1), wt.to(dev), G, R)
+    torch.cuda.synchronize()
+    assert k.dsv4_device_status(clear=True) == 0
+    _, z64 = oracle.grouped_gemm_bf16(x, wt, T, G, D, R, want_fp64=True)
+    assert gemm_rel_err(to_bits(z), z64) <= GEMM_RTOL
+
+
+def test_bf16_path_chain_on_decode(dev):
+    """grouped_input then the bmm path, as deep_gemm_fp8_o_proj runs them for a
+    bf16 wo_a, against the oracle chain."""
+    import deepseek_v4_attention_gb300 as k
+    w = di.WORKLOADS["decode"]
+    d = di.make_inputs(w, with_wo_b=False)
+    rng = np.random.default_rng(5)
+    wt = torch.from_numpy(rng.standard_normal((w.n_groups * w.o_lora_rank, w.D)).astype(
+        np.float32) * 0.02).to(torch.bfloat16)
+    x = k.dsv4_inv_rope_bf16(d["o"].to(dev), d["positions"].to(dev), d["cache"].to(dev),
+                             w.n_groups, w.heads_per_group)
+    z = k.dsv4_grouped_wo_a_bf16(x, wt.to(dev), w.n_groups, w.o_lora_rank)
+    torch.cuda.synchronize()
+    xr = oracle.inv_rope_bf16(d["o"], d["positions"], d["cache"], w.n_groups, w.heads_per_group)
+    _, z64 = oracle.grouped_gemm_bf16(xr, wt, w.T, w.n_groups, w.D, w.o_lora_rank, want_fp64=True)
+    assert gemm_rel_err(to_bits(z), z64) <= GEMM_RTOL
