@@ -47,7 +47,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--workload", default="full",
-                    choices=["full", "tiny", "decode", "prefill", "quant1k", "quant8k", "quant32k"],
+                    choices=["full", "tiny", "decode", "prefill", "quant1k", "quant8k", "quant32k",
+                             "decode_bf16", "prefill_bf16"],
                     help="full: the O-projection (default); decode / prefill: quant + grouped "
                          "wo_a; quantNk: the quantiser alone (timed by CUDA-graph replay over "
                          "rotating input sets)")
@@ -423,18 +424,23 @@ def run_workload(args, ws, rank, local):
         raise SystemExit("--workload other than full runs on one GPU")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = di.WORKLOADS[args.workload]
+    bf16 = args.workload.endswith("_bf16")
+    w = di.WORKLOADS[args.workload.replace("_bf16", "")]
     gemm = not w.name.startswith("quant")
     host = di.make_inputs(w, with_wo_b=False)
+    if bf16:   # the model served without FP8: bf16 wo_a, quantize=False
+        host["wo_a"] = di.bf16_weight(w.n_groups * w.o_lora_rank, w.D, w.seed + 303)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    set_bytes = host["o"].numel() * 2 + (host["wo_a"].numel() if gemm else 0) + \
-        w.n_groups * w.T * w.D + (w.T * w.n_groups * w.o_lora_rank * 2 if gemm else 0)
+    esz = 2 if bf16 else 1
+    set_bytes = host["o"].numel() * 2 + (host["wo_a"].numel() * esz if gemm else 0) + \
+        w.n_groups * w.T * w.D * esz + (w.T * w.n_groups * w.o_lora_rank * 2 if gemm else 0)
     nsets = max(1, min(32, -(-3 * l2 // set_bytes)))
     T_al = k.tma_aligned_tokens(w.T)
     sets = []
     for i in range(nsets):
         st = {n: host[n].to(dev) for n in ("o", "positions", "cache")}
-        st["x"] = torch.empty(w.n_groups, w.T, w.D, dtype=torch.float8_e4m3fn, device=dev)
+        st["x"] = torch.empty(w.n_groups, w.T, w.D, dtype=torch.bfloat16 if bf16
+                              else torch.float8_e4m3fn, device=dev)
         st["xs"] = torch.empty(w.n_groups, (w.D // 128 + 3) // 4, T_al, dtype=torch.int32,
                                device=dev)
         if gemm:
@@ -447,12 +453,19 @@ def run_workload(args, ws, rank, local):
 
     def quant(i):
         st = sets[i % nsets]
+        if bf16:
+            return k.dsv4_inv_rope_bf16(st["o"], st["positions"], st["cache"], w.n_groups,
+                                        w.heads_per_group, out=st["x"], stream=stream)
         return k.dsv4_inv_rope_fp8_quant(st["o"], st["positions"], st["cache"], w.n_groups,
                                          w.heads_per_group, out_fp8=st["x"], out_scale=st["xs"],
                                          stream=stream)
 
     def wo_a(i):
         st = sets[i % nsets]
+        if bf16:
+            k.dsv4_grouped_wo_a_bf16(st["x"].transpose(0, 1), st["wo_a"], w.n_groups,
+                                     w.o_lora_rank, z=st["z"], stream=stream)
+            return
         k.dsv4_grouped_wo_a(st["x"].transpose(0, 1), st["xs"].permute(2, 0, 1)[:w.T],
                             st["wo_a"], st["wo_a_scale"], w.n_groups, w.o_lora_rank, z=st["z"],
                             stream=stream)
@@ -474,14 +487,16 @@ def run_workload(args, ws, rank, local):
     if k.dsv4_device_status(clear=True) != 0:
         raise RuntimeError("device status error")
     peaks, src = measured_peaks()
-    qbytes = w.T * w.H * (1024 + 512 + 4) + w.T * (8 + 256)
+    qbytes = w.T * w.H * (1024 + (1024 if bf16 else 512 + 4)) + w.T * (8 + 256)
     stages = {"quant": {"ms": ms_q, "bound": "hbm", "algorithmic": qbytes,
                         "achieved": qbytes / (ms_q * 1e-3) / 1e9, "unit": "GB/s",
                         "peak": peaks["hbm_gbs"]}}
     if gemm:
         fl = 2.0 * w.T * w.n_groups * w.o_lora_rank * w.D
-        by = w.n_groups * w.o_lora_rank * w.D + w.n_groups * w.T * w.D + \
+        by = (w.n_groups * w.o_lora_rank * w.D + w.n_groups * w.T * w.D) * esz + \
             w.T * w.n_groups * w.o_lora_rank * 2
+        tensor_peak = (1.0 if bf16 else 2.0) * peaks.get("bf16_tflops_sustained",
+                                                          peaks["bf16_tflops"])
         if w.name == "decode":      # weight-read bound: bytes against HBM
             stages["wo_a"] = {"ms": ms_a, "bound": "hbm", "algorithmic": by,
                               "achieved": by / (ms_a * 1e-3) / 1e9, "unit": "GB/s",
@@ -489,8 +504,7 @@ def run_workload(args, ws, rank, local):
         else:
             stages["wo_a"] = {"ms": ms_a, "bound": "tensor", "algorithmic": fl,
                               "achieved": fl / (ms_a * 1e-3) / 1e12, "unit": "TFLOP/s",
-                              "peak": 2.0 * peaks.get("bf16_tflops_sustained",
-                                                      peaks["bf16_tflops"])}
+                              "peak": tensor_peak}
     for s_ in stages.values():
         s_["frac"] = s_["achieved"] / s_["peak"]
     dom = max(stages, key=lambda n: stages[n]["ms"])
@@ -498,11 +512,15 @@ def run_workload(args, ws, rank, local):
     result = {
         "metric": METRIC, "value": w.T / (ms_step * 1e-3), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-        "data": "synthetic (seeded; random FP8 block-scaled weights)",
-        "config": {"workload": f"{w.name}: T={w.T}, {w.H} heads x 512 ({w.n_groups} groups x "
-                               f"{w.heads_per_group})" + (f", o_lora_rank {w.o_lora_rank}, "
-                               "quant + grouped wo_a" if gemm else ", quantiser alone"),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if bf16 else "e4m3",
+        "data": "synthetic (seeded; random " + ("bf16" if bf16 else "FP8 block-scaled") +
+                " weights)",
+        "config": {"workload": f"{args.workload}: T={w.T}, {w.H} heads x 512 ({w.n_groups} "
+                               f"groups x {w.heads_per_group})" +
+                               (f", o_lora_rank {w.o_lora_rank}, " + ("bf16 inverse RoPE + bf16 "
+                                "grouped wo_a" if bf16 else "quant + grouped wo_a")
+                                if gemm else ", quantiser alone"),
                    "timing": "CUDA-graph replay", "input_sets": nsets,
                    "l2": f"{nsets} rotating input sets of {set_bytes / 1e6:.1f} MB (>= 3x L2)"},
         "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,

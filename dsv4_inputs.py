@@ -149,6 +149,13 @@ def fp8_block_weight(rows: int, cols: int, seed: int):
     return codes, scale
 
 
+def bf16_weight(rows: int, cols: int, seed: int) -> torch.Tensor:
+    """bf16 [rows, cols] drawn N(0, 0.02): the wo_a of a model served without FP8."""
+    gen = _gen(seed)
+    return (torch.randn((rows, cols), generator=gen, dtype=torch.float32) * 0.02).to(
+        torch.bfloat16).contiguous()
+
+
 def make_inputs(w: Workload, with_wo_b: bool = True) -> dict:
     """All CPU tensors of one workload: o, positions, cache, wo_a (+ wo_b)."""
     gen = _gen(w.seed)
