@@ -332,6 +332,12 @@ int dsv4_o_proj_with_events(const void* o, const int64_t* positions, const float
   a.epilogue = kEpiQuant;
   a.q_out = zq;
   a.q_scale = zs;
+  // Programmatic launches overlap a GEMM's prologue and first weight loads with
+  // the previous kernel's tail: measured -2 % time at T <= 512 and +0.6 % at
+  // T = 4096, so only for small calls (and never when stage events are asked
+  // for, whose per-kernel times would then overlap).
+  const bool overlap = stage_events == nullptr && T <= 2048;
+  a.after_own_kernel = overlap;
   if ((rc = launch_block_scaled_gemm(a, s, dev)) != DSV4_OK) return rc;
   if (!mark(2)) return DSV4_ERR_CUDA;
 
@@ -346,6 +352,7 @@ int dsv4_o_proj_with_events(const void* o, const int64_t* positions, const float
   b.b_scale = wo_b_scale;
   b.epilogue = kEpiBf16;
   b.out_bf16 = out;
+  b.after_own_kernel = overlap;
   if ((rc = launch_block_scaled_gemm(b, s, dev)) != DSV4_OK) return rc;
   if (!mark(3)) return DSV4_ERR_CUDA;
   t_last_launches = 3;

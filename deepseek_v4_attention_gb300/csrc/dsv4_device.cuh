@@ -162,6 +162,20 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialization may start while the
+// previous kernel of the stream still runs; griddep_wait() blocks until that
+// kernel has completed and its memory is visible (a no-op for a normal launch).
+// griddep_launch_dependents() lets the next such kernel start once every CTA of
+// this grid has executed it (or exited).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- clusters --
 __device__ __forceinline__ uint32_t cluster_cta_rank() {
   uint32_t r;

@@ -49,7 +49,6 @@ constexpr int kBM = 128;
 constexpr int kBK = 128;
 constexpr int kTmemCols = 512;
 
-constexpr uint32_t kABytes = kBM * kBK;    // 16 KiB
 constexpr uint32_t kSfaBytes = kBM * 4;    // 512 B
 
 // Tile configuration.  kBN = 128: two 128-column TMEM accumulators (the
@@ -57,9 +56,16 @@ constexpr uint32_t kSfaBytes = kBM * 4;    // 512 B
 // kBN = 256: one 256-column accumulator (N = 256 is the full-width single-SM
 // MMA), 8 epilogue warps that copy it to registers and release TMEM before
 // they convert and store, so the next tile's MMAs start almost at once.
-template <int kBN>
+//
+// kARows = 64 (tokens T <= 64, the decode shapes): only 64 A rows are loaded per
+// stage (8 KiB instead of 16); the MMA still reads a 128-row A tile, whose last
+// 64 rows (the next bytes of shared memory) only reach accumulator rows that
+// are never stored.  The smaller stage fits 8 stages instead of 6, a third more
+// weight bytes in flight per CTA.
+template <int kBN, int kARows = 128>
 struct Cfg {
-  static constexpr int kStages = (kBN == 128) ? 6 : 4;
+  static constexpr uint32_t kABytes = kARows * kBK;
+  static constexpr int kStages = (kARows == 64) ? 8 : (kBN == 128) ? 6 : 4;
   static constexpr int kAccBufs = (kBN == 128) ? 2 : 1;
   static constexpr int kEpiWarps = (kBN == 128) ? 4 : 8;
   static constexpr int kEpiWarp0 = 3;
@@ -121,12 +127,13 @@ __device__ __forceinline__ uint32_t b_scale_word(const Params& p, int rb, int j)
   return w;
 }
 
-template <int kBN, int kEpi, int kSplit, bool kBf16>
-__global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
+template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows>
+__global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b,
                              const __grid_constant__ CUtensorMap tm_out, const Params p) {
-  using C = Cfg<kBN>;
+  using C = Cfg<kBN, kARows>;
+  constexpr uint32_t kABytes = C::kABytes;
   constexpr int kStages = C::kStages;
   constexpr int kAccBufs = C::kAccBufs;
   constexpr uint32_t kBBytes = C::kBBytes;
@@ -150,6 +157,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  griddep_launch_dependents();  // a following GEMM may start its prologue now
 
   // Split-K (kSplit > 1): a cluster of kSplit CTAs shares one output tile, CTA
   // r of the cluster taking k-blocks [r, r+1) * k_blocks / kSplit; otherwise a
@@ -199,12 +207,35 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // bit s: stage s loaded / parity of its phase
       bool ok = true;
+      // Before the previous kernel of the stream has finished (programmatic
+      // launch) only the weights may be read: the first stages of the first
+      // tile get their B tile now and their A tile after griddep_wait().
+      int early = 0;
+      if (tile0 < p.num_tiles) {
+        int g, n_blk, m_blk;
+        tile_coords(p, tile0, g, n_blk, m_blk);
+        const int brow = g * p.N + n_blk * kBN;
+        early = (kb1 - kb0) < kStages ? (kb1 - kb0) : kStages;
+        for (int i = 0; i < early; ++i) {
+          mbar_arrive_expect_tx(&full[i], kABytes + kBBytes);
+          tma_load_2d(smem + C::b + i * kBBytes, &tm_b, &full[i], (kb0 + i) * kBKe, brow);
+        }
+      }
+      griddep_wait();
       for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
         int g, n_blk, m_blk;
         tile_coords(p, tile, g, n_blk, m_blk);
         const int m0 = m_blk * kBM;
         const int brow = g * p.N + n_blk * kBN;
         for (int kb = kb0; kb < kb1; ++kb) {
+          if (early > 0) {  // B already in flight for this stage
+            tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBKe, m0, g);
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            --early;
+            continue;
+          }
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
           tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBKe, m0, g);
@@ -304,6 +335,7 @@ __global__ void __launch_bounds__(Cfg<kBN>::kThreads, 1)
         for (int i = 0; i < 4; ++i)
           if (lane + 32 * i < packs) wnext[r][i] = b_scale_word(p, rb + r, lane + 32 * i);
     }
+    griddep_wait();  // the A scale words are written by the previous kernel
     uint32_t n = 0;  // packs staged so far (all tiles)
     bool ok = true;
     for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
@@ -550,13 +582,16 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kBN, int kEpi, int kSplit, bool kBf16>
+template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows>
 int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
-  using C = Cfg<kBN>;
+  // q.after_own_kernel: the previous kernel on the stream is one of this
+  // library's (inside dsv4_o_proj), so the launch may overlap it: this kernel
+  // reads only weights before griddep_wait().
+  using C = Cfg<kBN, kARows>;
   static int configured_for[64] = {0};
   if (dev.device < 0 || dev.device >= 64) return DSV4_ERR_UNSUPPORTED;
   if (!configured_for[dev.device]) {
-    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16>,
+    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::smem_bytes)) != cudaSuccess)
       return DSV4_ERR_CUDA;
@@ -577,7 +612,7 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
                           static_cast<cuuint64_t>(q.G)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.K) * esz,
                              static_cast<cuuint64_t>(T * q.K) * esz};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(kbe), kBM, 1};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kbe), static_cast<cuuint32_t>(kARows), 1};
     if (!encode(&tm_a, dt, 3, q.a, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return DSV4_ERR_CUDA;
   }
@@ -620,27 +655,32 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   p.q_scale = q.q_scale;
   p.status = dev.status;
 
-  if (kSplit == 1) {
-    const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
-    block_scaled_gemm_kernel<kBN, kEpi, 1, kBf16>
-        <<<grid, C::kThreads, C::smem_bytes, stream>>>(tm_a, tm_b, tm_out, p);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
-  }
-  // one cluster of kSplit CTAs per output tile
+  // persistent: one CTA per SM; split-K: one cluster of kSplit CTAs per tile
+  const int grid = kSplit == 1 ? (p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms)
+                               : p.num_tiles * kSplit;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles * kSplit));
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kSplit;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (kSplit > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = kSplit;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (q.after_own_kernel) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16>, tm_a, tm_b,
-                         tm_out, p) != cudaSuccess)
+  cfg.numAttrs = na;
+  if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows>, tm_a,
+                         tm_b, tm_out, p) != cudaSuccess)
     return DSV4_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
@@ -659,22 +699,36 @@ int launch_block_scaled_gemm(const GemmProblem& q, cudaStream_t stream, const De
   const int64_t tiles = m_tiles * (q.N / 128) * q.G;
   const int kbs = q.bf16 ? q.K / 64 : q.K / 128;
   const bool split = !wide && kbs % (q.bf16 ? 2 : 8) == 0 && 2 * tiles <= dev.num_sms;
+  // at most 64 tokens: one m-tile with a 64-row A box (see Cfg)
+  const bool small_m = !wide && q.T <= 64;
   if (q.bf16) {
     if (q.epilogue != kEpiBf16) return DSV4_ERR_UNSUPPORTED;
-    if (wide) return launch_impl<256, kEpiBf16, 1, true>(q, stream, dev);
-    if (split) return launch_impl<128, kEpiBf16, 2, true>(q, stream, dev);
-    return launch_impl<128, kEpiBf16, 1, true>(q, stream, dev);
+    if (wide) return launch_impl<256, kEpiBf16, 1, true, 128>(q, stream, dev);
+    if (small_m) {
+      if (split) return launch_impl<128, kEpiBf16, 2, true, 64>(q, stream, dev);
+      return launch_impl<128, kEpiBf16, 1, true, 64>(q, stream, dev);
+    }
+    if (split) return launch_impl<128, kEpiBf16, 2, true, 128>(q, stream, dev);
+    return launch_impl<128, kEpiBf16, 1, true, 128>(q, stream, dev);
   }
   if (wide) {
-    if (q.epilogue == kEpiQuant) return launch_impl<256, kEpiQuant, 1, false>(q, stream, dev);
-    return launch_impl<256, kEpiBf16, 1, false>(q, stream, dev);
+    if (q.epilogue == kEpiQuant) return launch_impl<256, kEpiQuant, 1, false, 128>(q, stream, dev);
+    return launch_impl<256, kEpiBf16, 1, false, 128>(q, stream, dev);
+  }
+  if (small_m) {
+    if (split) {
+      if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 2, false, 64>(q, stream, dev);
+      return launch_impl<128, kEpiBf16, 2, false, 64>(q, stream, dev);
+    }
+    if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 1, false, 64>(q, stream, dev);
+    return launch_impl<128, kEpiBf16, 1, false, 64>(q, stream, dev);
   }
   if (split) {
-    if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 2, false>(q, stream, dev);
-    return launch_impl<128, kEpiBf16, 2, false>(q, stream, dev);
+    if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 2, false, 128>(q, stream, dev);
+    return launch_impl<128, kEpiBf16, 2, false, 128>(q, stream, dev);
   }
-  if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 1, false>(q, stream, dev);
-  return launch_impl<128, kEpiBf16, 1, false>(q, stream, dev);
+  if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 1, false, 128>(q, stream, dev);
+  return launch_impl<128, kEpiBf16, 1, false, 128>(q, stream, dev);
 }
 
 }  // namespace dsv4

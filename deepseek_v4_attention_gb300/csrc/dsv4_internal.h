@@ -34,6 +34,8 @@ struct GemmProblem {
   const uint8_t* b_scale = nullptr; // UE8M0 bytes [G*N/128][K/128]
   int epilogue = kEpiBf16;
   bool bf16 = false;                // A and B bf16, no scales (kind::f16), K % 64 == 0
+  bool after_own_kernel = false;    // previous kernel on the stream is this library's own:
+                                    // launch with programmatic stream serialization
   void* out_bf16 = nullptr;         // bf16 [T][G*N] (kEpiBf16)
   uint8_t* q_out = nullptr;         // e4m3 [T][G*N]           (kEpiQuant)
   int32_t* q_scale = nullptr;       // int32 [ceil(G*N/512)][T_al] (kEpiQuant)

@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(256) inv_rope_fp8_quant_kernel(
     const float* __restrict__ cache, int64_t T, int64_t max_pos, int H, int hpg,
     uint8_t* __restrict__ out_fp8, int32_t* __restrict__ out_scale, int64_t T_al,
     int* __restrict__ status) {
+  griddep_launch_dependents();  // a following GEMM may start its prologue now
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
