@@ -5,7 +5,15 @@ Tolerances (written out here and used by every GEMM parity test):
   - UE8M0 scale bytes: bit-exact.
   - FP8 codes: at least 99.99% bit-exact, every other code within one E4M3 step.
   - GEMM outputs (z, out): max_i |gpu_i - ref_i| / max(|ref_i|, rms(ref)) <= 1e-2,
-    with ref the fp64-accumulated product of the dequantised operands.
+    with ref the fp64-accumulated product of the dequantised operands, when the
+    GPU and the oracle multiply the same FP8 operands (every GEMM test on oracle
+    inputs, and wo_a inside the chain).
+  - The chained O-projection (out after the z re-quantisation): the GPU rounds
+    z to bf16 from an fp32 tensor-core sum, the oracle from an fp64 sum, so a z
+    within an fp32 rounding error of a bf16 tie may round the other way and move
+    one FP8 code of zq by one step; both are results of the method.  As for the
+    FP8 codes: at least 99.99 % of the outputs within 1e-2, every output within
+    3e-2 (CHAIN_RTOL_ALL).
 """
 from __future__ import annotations
 
@@ -15,6 +23,8 @@ import torch
 
 GEMM_RTOL = 1e-2
 CODE_EXACT_MIN = 0.9999
+CHAIN_WITHIN_MIN = 0.9999
+CHAIN_RTOL_ALL = 3e-2
 
 
 def cuda_or_skip():
@@ -61,3 +71,19 @@ def to_bits(t: torch.Tensor) -> np.ndarray:
     if t.element_size() == 1:
         return t.view(torch.uint8).numpy()
     return t.numpy()
+
+
+def chain_rel_errs(gpu_bf16_bits: np.ndarray, ref64: np.ndarray) -> np.ndarray:
+    g = torch.from_numpy(np.ascontiguousarray(gpu_bf16_bits).view(np.int16)).view(
+        torch.bfloat16).to(torch.float64).numpy()
+    ref = ref64.astype(np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 1.0
+    return np.abs(g - ref) / np.maximum(np.abs(ref), rms)
+
+
+def assert_chain_matches(gpu_bf16_bits: np.ndarray, ref64: np.ndarray, what: str = "out"):
+    err = chain_rel_errs(gpu_bf16_bits, ref64)
+    within = float((err <= GEMM_RTOL).mean()) if err.size else 1.0
+    assert within >= CHAIN_WITHIN_MIN, f"{what}: only {within:.6f} within {GEMM_RTOL}"
+    assert float(err.max(initial=0.0)) <= CHAIN_RTOL_ALL, f"{what}: max {err.max()}"
+    return within, float(err.max(initial=0.0))

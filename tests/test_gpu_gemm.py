@@ -6,7 +6,8 @@ import torch
 
 import dsv4_inputs as di
 import oracle
-from gpu_helpers import GEMM_RTOL, assert_codes_match, cuda_or_skip, gemm_rel_err, to_bits
+from gpu_helpers import (GEMM_RTOL, assert_chain_matches, assert_codes_match, cuda_or_skip,
+                         gemm_rel_err, to_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -136,7 +137,7 @@ def test_o_proj_tiny_parity(dev, T):
                                 d["wo_b"], d["wo_b_scale"], n_groups=w.n_groups,
                                 heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank,
                                 hidden=w.hidden)
-    assert gemm_rel_err(og, out64) <= GEMM_RTOL
+    assert_chain_matches(og, out64)
 
 
 def test_o_proj_full_config_sampled(dev):
@@ -152,7 +153,7 @@ def test_o_proj_full_config_sampled(dev):
                                 d["wo_a_scale"], d["wo_b"], d["wo_b_scale"], n_groups=w.n_groups,
                                 heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank,
                                 hidden=w.hidden)
-    assert gemm_rel_err(og[idx], out64) <= GEMM_RTOL
+    assert_chain_matches(og[idx], out64)
     og2 = _o_proj_gpu(d, w, dev)
     assert np.array_equal(og, og2), "two runs differ"
 
@@ -264,3 +265,29 @@ def test_bf16_path_chain_on_decode(dev):
     xr = oracle.inv_rope_bf16(d["o"], d["positions"], d["cache"], w.n_groups, w.heads_per_group)
     _, z64 = oracle.grouped_gemm_bf16(xr, wt, w.T, w.n_groups, w.D, w.o_lora_rank, want_fp64=True)
     assert gemm_rel_err(to_bits(z), z64) <= GEMM_RTOL
+
+
+def _random_o_proj_case(i):
+    import dataclasses
+    rng = np.random.default_rng(4242 + i)
+    G = int(rng.integers(1, 5))
+    hpg = int(rng.integers(1, 4))
+    R = 128 * int(rng.integers(1, 4))
+    hidden = 128 * int(rng.integers(1, 5))
+    T = int(rng.choice([1, 2, 17, 63, 64, 65, 127, 200, 300]))
+    return dataclasses.replace(di.WORKLOADS["tiny"], T=T, n_groups=G, heads_per_group=hpg,
+                               o_lora_rank=R, hidden=hidden, seed=5000 + i)
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_o_proj_random_shapes(dev, i):
+    """Seeded random (T, G, hpg, R, hidden): every tile path (128 / 256 wide,
+    split-K, 64-row A box, ragged T) against the oracle's whole chain."""
+    w = _random_o_proj_case(i)
+    d = di.make_inputs(w)
+    og = _o_proj_gpu(d, w, dev)
+    _, out64, _ = oracle.o_proj(d["o"], d["positions"], d["cache"], d["wo_a"], d["wo_a_scale"],
+                                d["wo_b"], d["wo_b_scale"], n_groups=w.n_groups,
+                                heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank,
+                                hidden=w.hidden)
+    assert_chain_matches(og, out64, what=str(w))

@@ -162,3 +162,13 @@ def test_pipeline_wait_timeout_is_reported_not_trapped(dev):
     assert k.dsv4_device_status(clear=True) == k._NAME_TO_CODE["DSV4_ERR_TIMEOUT"]
     assert k.dsv4_device_status(clear=True) == 0
     _compare(di.WORKLOADS["tiny"], dev)
+
+
+@pytest.mark.parametrize("G,hpg,T", [(1, 1, 7), (1, 2, 33), (3, 1, 5), (3, 2, 130), (2, 3, 9)])
+def test_quant_parity_odd_head_counts(dev, G, hpg, T):
+    """H = G * hpg not a multiple of 4 (the 1- and 2-head-per-iteration paths)."""
+    import dataclasses
+    w = dataclasses.replace(di.WORKLOADS["tiny"], T=T, n_groups=G, heads_per_group=hpg,
+                            seed=1000 + 10 * G + hpg)
+    frac = _compare(w, dev)
+    assert frac == 1.0
