@@ -127,6 +127,33 @@ __device__ __forceinline__ uint32_t b_scale_word(const Params& p, int rb, int j)
   return w;
 }
 
+// Tile schedule.  kSplit = 1: a persistent CTA walks tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ... over all k-blocks.  kSplit > 1: a cluster of
+// kSplit CTAs shares one output tile, CTA r of the cluster taking k-blocks
+// [r, r+1) * k_blocks / kSplit.  Each role evaluates these where it uses them:
+// values computed once above the role dispatch stay live through every role
+// and cost the tensor pipe a few per cent (measured).
+template <int kSplit>
+__device__ __forceinline__ int split_rank() {
+  return kSplit > 1 ? static_cast<int>(cluster_cta_rank()) : 0;
+}
+template <int kSplit>
+__device__ __forceinline__ int first_tile() {
+  return kSplit > 1 ? static_cast<int>(blockIdx.x) / kSplit : static_cast<int>(blockIdx.x);
+}
+template <int kSplit>
+__device__ __forceinline__ int tile_stride(const Params& p) {
+  return kSplit > 1 ? p.num_tiles : static_cast<int>(gridDim.x);
+}
+template <int kSplit>
+__device__ __forceinline__ int kb_begin(const Params& p) {
+  return kSplit > 1 ? split_rank<kSplit>() * (p.k_blocks / kSplit) : 0;
+}
+template <int kSplit>
+__device__ __forceinline__ int kb_end(const Params& p) {
+  return kSplit > 1 ? kb_begin<kSplit>(p) + p.k_blocks / kSplit : p.k_blocks;
+}
+
 template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows>
 __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
@@ -159,15 +186,6 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   griddep_launch_dependents();  // a following GEMM may start its prologue now
 
-  // Split-K (kSplit > 1): a cluster of kSplit CTAs shares one output tile, CTA
-  // r of the cluster taking k-blocks [r, r+1) * k_blocks / kSplit; otherwise a
-  // persistent loop over tiles.
-  const int split_rank = (kSplit > 1) ? static_cast<int>(cluster_cta_rank()) : 0;
-  const int tile0 = (kSplit > 1) ? static_cast<int>(blockIdx.x) / kSplit
-                                 : static_cast<int>(blockIdx.x);
-  const int tile_step = (kSplit > 1) ? p.num_tiles : static_cast<int>(gridDim.x);
-  const int kb0 = split_rank * (p.k_blocks / kSplit);
-  const int kb1 = kb0 + p.k_blocks / kSplit;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -211,23 +229,26 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
       // launch) only the weights may be read: the first stages of the first
       // tile get their B tile now and their A tile after griddep_wait().
       int early = 0;
-      if (tile0 < p.num_tiles) {
+      if (first_tile<kSplit>() < p.num_tiles) {
         int g, n_blk, m_blk;
-        tile_coords(p, tile0, g, n_blk, m_blk);
+        tile_coords(p, first_tile<kSplit>(), g, n_blk, m_blk);
         const int brow = g * p.N + n_blk * kBN;
-        early = (kb1 - kb0) < kStages ? (kb1 - kb0) : kStages;
+        const int kbs = kb_end<kSplit>(p) - kb_begin<kSplit>(p);
+        early = kbs < kStages ? kbs : kStages;
         for (int i = 0; i < early; ++i) {
           mbar_arrive_expect_tx(&full[i], kABytes + kBBytes);
-          tma_load_2d(smem + C::b + i * kBBytes, &tm_b, &full[i], (kb0 + i) * kBKe, brow);
+          tma_load_2d(smem + C::b + i * kBBytes, &tm_b, &full[i],
+                      (kb_begin<kSplit>(p) + i) * kBKe, brow);
         }
       }
       griddep_wait();
-      for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
+      for (int tile = first_tile<kSplit>(); tile < p.num_tiles && ok;
+           tile += tile_stride<kSplit>(p)) {
         int g, n_blk, m_blk;
         tile_coords(p, tile, g, n_blk, m_blk);
         const int m0 = m_blk * kBM;
         const int brow = g * p.N + n_blk * kBN;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb_begin<kSplit>(p); kb < kb_end<kSplit>(p); ++kb) {
           if (early > 0) {  // B already in flight for this stage
             tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBKe, m0, g);
             issued |= 1u << stage;
@@ -257,22 +278,25 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
       const uint64_t adesc0 = smem_desc(smem_addr(smem + C::a), 16, 1024, 2);
       const uint64_t bdesc0 = smem_desc(smem_addr(smem + C::b), 16, 1024, 2);
       const uint64_t sfdesc0 = smem_desc(smem_addr(smem + C::sf), 0, 128, 0);
-      uint32_t idesc[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) idesc[i] = kBf16 ? bf16_idesc(kBM, kBN) : mxf8_idesc(kBM, kBN, i, i);
+      // The scale-factor id (the k-block within its pack of four) selects the
+      // byte of the packed scale words: fields [4,6) (B) and [29,31) (A) of the
+      // instruction descriptor, set arithmetically (an indexed array of four
+      // descriptors would live in local memory).
+      const uint32_t idesc0 = kBf16 ? bf16_idesc(kBM, kBN) : mxf8_idesc(kBM, kBN, 0, 0);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       uint32_t packs_done = 0;  // scale-factor packs consumed so far (all tiles)
       bool ok = true;
-      for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
+      for (int tile = first_tile<kSplit>(); tile < p.num_tiles && ok;
+           tile += tile_stride<kSplit>(p)) {
         if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
         uint32_t sf_col = 0;
         int slot = 0;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb_begin<kSplit>(p); kb < kb_end<kSplit>(p); ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           if (!kBf16 && (kb & 3) == 0) {
@@ -290,20 +314,22 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
           }
           const uint64_t ad = adesc0 + ((stage * kABytes) >> 4);
           const uint64_t bd = bdesc0 + ((stage * kBBytes) >> 4);
-          const uint32_t id = idesc[kb & 3];
+          const uint32_t sfid = kBf16 ? 0u : static_cast<uint32_t>(kb & 3);
+          const uint32_t id = idesc0 | (sfid << 4) | (sfid << 29);
           // four MMAs per k-block: K = 32 e4m3 or K = 16 bf16, 32 bytes each
           // (+32 bytes along K = +2 in the descriptor's address field)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             if constexpr (kBf16)
-              mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, id, ((kb - kb0) | k) != 0 ? 1u : 0u);
+              mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, id,
+                       ((kb - kb_begin<kSplit>(p)) | k) != 0 ? 1u : 0u);
             else
               mma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, id, sf_col, sf_col + 4,
-                       ((kb - kb0) | k) != 0 ? 1u : 0u);
+                       ((kb - kb_begin<kSplit>(p)) | k) != 0 ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
           // the last k-block that reads this scale-factor slot releases it
-          if (!kBf16 && ((kb & 3) == 3 || kb == kb1 - 1)) mma_commit(&sf_empty[slot]);
+          if (!kBf16 && ((kb & 3) == 3 || kb == kb_end<kSplit>(p) - 1)) mma_commit(&sf_empty[slot]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -325,9 +351,9 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
     for (int r = 0; r < kRb; ++r)
 #pragma unroll
       for (int i = 0; i < 4; ++i) wnext[r][i] = 0u;
-    if (tile0 < p.num_tiles) {
+    if (first_tile<kSplit>() < p.num_tiles) {
       int g, nb, mb;
-      tile_coords(p, tile0, g, nb, mb);
+      tile_coords(p, first_tile<kSplit>(), g, nb, mb);
       const int rb = (g * p.N + nb * kBN) / 128;
 #pragma unroll
       for (int r = 0; r < kRb; ++r)
@@ -338,7 +364,8 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
     griddep_wait();  // the A scale words are written by the previous kernel
     uint32_t n = 0;  // packs staged so far (all tiles)
     bool ok = true;
-    for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
+    for (int tile = first_tile<kSplit>(); tile < p.num_tiles && ok;
+         tile += tile_stride<kSplit>(p)) {
       int g, n_blk, m_blk;
       tile_coords(p, tile, g, n_blk, m_blk);
       uint32_t wcur[kRb][4];
@@ -346,7 +373,7 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
       for (int r = 0; r < kRb; ++r)
 #pragma unroll
         for (int i = 0; i < 4; ++i) wcur[r][i] = wnext[r][i];
-      const int next = tile + tile_step;
+      const int next = tile + tile_stride<kSplit>(p);
       if (next < p.num_tiles) {
         int g2, nb2, mb2;
         tile_coords(p, next, g2, nb2, mb2);
@@ -358,7 +385,7 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
             wnext[r][i] = (lane + 32 * i < packs) ? b_scale_word(p, rb2 + r, lane + 32 * i) : 0u;
       }
       const int64_t m0 = static_cast<int64_t>(m_blk) * kBM;
-      for (int j = kb0 / 4; j < (kb1 + 3) / 4; ++j) {
+      for (int j = kb_begin<kSplit>(p) / 4; j < (kb_end<kSplit>(p) + 3) / 4; ++j) {
         // the 128 scale words of this pack: lane r takes rows r, r+32, r+64, r+96
         const int32_t* src = p.a_scale + (static_cast<int64_t>(g) * packs + j) * p.t_al + m0;
         uint32_t v[4];
@@ -394,7 +421,8 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool synced = false;  // split-K: this warp took part in the two cluster barriers
-    for (int tile = tile0; tile < p.num_tiles; tile += tile_step) {
+    for (int tile = first_tile<kSplit>(); tile < p.num_tiles;
+         tile += tile_stride<kSplit>(p)) {
       int g, n_blk, m_blk;
       tile_coords(p, tile, g, n_blk, m_blk);
       if (!mbar_wait_warp(&tmem_full[acc], acc_phase, abort_flag, p.status)) break;
@@ -420,7 +448,7 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
         // (32 rows x 128 fp32) has its own 16 KiB there, laid out [col/4][lane].
         cluster_sync();
         const uint32_t part = smem_addr(smem + C::a) + static_cast<uint32_t>(epi) * 16384u;
-        if (split_rank != 0) {
+        if (split_rank<kSplit>() != 0) {
           const uint32_t dst = map_to_cta(part, 0);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -431,7 +459,7 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
         }
         cluster_sync();
         synced = true;
-        if (split_rank == 0) {
+        if (split_rank<kSplit>() == 0) {
           for (int peer = 1; peer < kSplit; ++peer) {
             const float4* src = reinterpret_cast<const float4*>(smem + C::a + epi * 16384);
 #pragma unroll
@@ -447,7 +475,7 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
           }
         }
       }
-      if (split_rank == 0) {
+      if (split_rank<kSplit>() == 0) {
       // Stores go through this warp's staging buffer: each lane writes its row's
       // 64-byte chunk with the 64-byte TMA swizzle (16-byte unit q of row r at
       // q ^ ((r >> 1) & 3): conflict-free), then one lane stores the 32-row box
@@ -525,7 +553,7 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
           sbytes[((blk >> 2) * p.t_al + t) * 4 + (blk & 3)] = static_cast<uint8_t>(e + 127);
         }
       }
-      }  // split_rank == 0
+      }  // split rank 0
       if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
     }
     if (lane == 0) bulk_wait_all();   // every store complete before the CTA leaves
