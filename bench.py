@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -369,8 +370,39 @@ def _oracle_tokens(w: di.Workload, host: dict, idx, oracle):
                   heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank, hidden=w.hidden)
 
 
+def _oracle_stages(w: di.Workload, host: dict, idx, oracle) -> dict:
+    """The same O-projection as _oracle_tokens, stage by stage (O-1 quant, O-2
+    grouped wo_a, O-3 z re-quant + wo_b); returns each stage's seconds."""
+    ti = torch.as_tensor(idx)
+    T = len(idx)
+    G, R, D = w.n_groups, w.o_lora_rank, w.D
+    t0 = time.perf_counter()
+    x, xs = oracle.inv_rope_fp8_quant(host["o"][ti], host["positions"][ti], host["cache"],
+                                      G, w.heads_per_group)
+    t1 = time.perf_counter()
+    z = oracle.grouped_gemm(x, xs, host["wo_a"], host["wo_a_scale"], T, G, D, R)
+    t2 = time.perf_counter()
+    zq, zs = oracle.block_quant_rows(z.reshape(T, G * R))
+    oracle.grouped_gemm(zq, zs, host["wo_b"], host["wo_b_scale"], T, 1, G * R, w.hidden)
+    t3 = time.perf_counter()
+    return {"quant": t1 - t0, "wo_a": t2 - t1, "wo_b": t3 - t2}
+
+
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(w: di.Workload, seconds: float, host: dict | None = None) -> dict:
-    """The oracle as it stands, on a bounded token sample of the same workload."""
+    """The oracle as it stands, on a bounded token sample of the same workload:
+    the whole O-projection on all host threads (the reported value), its stages
+    separately, and a one-thread run on a small sub-sample."""
     import oracle
     host = host or di.make_inputs(w)
     threads = oracle.num_threads()
@@ -383,9 +415,29 @@ def cpu_baseline(w: di.Workload, seconds: float, host: dict | None = None) -> di
     t = time.perf_counter()
     _oracle_tokens(w, host, list(range(m)), oracle)
     el = time.perf_counter() - t
+    # stage by stage on a quarter of the sample, then one thread on 8 tokens
+    ms_ = max(threads, m // 4 // threads * threads)
+    st = _oracle_stages(w, host, list(range(ms_)), oracle)
+    quant_bytes = w.H * (2 * w.head_dim + w.head_dim + 4) + 8 + 4 * w.rope_dim
+    work = {"quant": (quant_bytes * ms_ / 1e9, "GB/s"),
+            "wo_a": (2.0 * ms_ * w.n_groups * w.o_lora_rank * w.D / 1e9, "GFLOP/s"),
+            "wo_b": (2.0 * ms_ * w.hidden * w.n_groups * w.o_lora_rank / 1e9, "GFLOP/s")}
+    stages = {k: {"s": round(v, 3), "tokens_per_s": ms_ / v,
+                  work[k][1]: work[k][0] / v} for k, v in st.items()}
+    one = min(8, w.T)
+    oracle.set_num_threads(1)
+    try:
+        t = time.perf_counter()
+        _oracle_tokens(w, host, list(range(one)), oracle)
+        el1 = time.perf_counter() - t
+    finally:
+        oracle.set_num_threads(threads)
     return {"value": m / el, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{m} of the workload's {w.T} tokens through the whole O-projection "
-                      f"(plain C, fp64 GEMMs), {el:.1f} s"}
+                      f"(plain C, fp64 GEMMs), {el:.1f} s; stages on {ms_} tokens; "
+                      f"one thread on {one} tokens",
+            "cpu_model": _cpu_model(), "stages": stages,
+            "one_thread": {"value": one / el1, "unit": UNIT}}
 
 
 def run_reference(args, ws, rank):
@@ -424,10 +476,12 @@ def run_reference(args, ws, rank):
 
 
 # ------------------------------------------------- per-workload reports --
-def _graph_ms(fn, steps: int, stream) -> float:
-    """Device time of `steps` calls of fn, captured in CUDA graphs and replayed
-    (no host launch overhead in the measurement)."""
-    chunk = min(steps, 100)
+def _graph_ms(fn, steps: int, stream) -> dict:
+    """Device time per call of fn over `steps` calls, captured in a CUDA graph of
+    10 calls and replayed (no host launch overhead in the measurement).  Each
+    replay is timed on its own: the mean over all calls, and the median, p10 and
+    p90 of the per-replay times per call."""
+    chunk = min(steps, 10)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(chunk):
@@ -436,14 +490,16 @@ def _graph_ms(fn, steps: int, stream) -> float:
     with torch.cuda.stream(stream):          # replay on the stream the events are on
         g.replay()
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        ev[0].record(stream)
+        for r in range(reps):
             g.replay()
-        e1.record(stream)
+            ev[r + 1].record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / (reps * chunk)
+    per = sorted(ev[r].elapsed_time(ev[r + 1]) / chunk for r in range(reps))
+    q = lambda f: per[min(reps - 1, int(f * reps))]
+    return {"ms": ev[0].elapsed_time(ev[reps]) / (reps * chunk), "p10_ms": q(0.1),
+            "p50_ms": q(0.5), "p90_ms": q(0.9)}
 
 
 def run_workload(args, ws, rank, local):
@@ -513,16 +569,19 @@ def run_workload(args, ws, rank, local):
     torch.cuda.synchronize()
     launches_per_step = 2 if gemm else 1
     with ClockSampler(local) as clk:
-        ms_step = _graph_ms(step, args.steps, stream)
-        ms_q = _graph_ms(quant, args.steps, stream)
-        ms_a = _graph_ms(wo_a, args.steps, stream) if gemm else 0.0
+        t_step = _graph_ms(step, args.steps, stream)
+        t_q = _graph_ms(quant, args.steps, stream)
+        t_a = _graph_ms(wo_a, args.steps, stream) if gemm else None
+    ms_step, ms_q = t_step["ms"], t_q["ms"]
+    ms_a = t_a["ms"] if gemm else 0.0
+    spread = lambda t: {k_: round(v, 5) for k_, v in t.items() if k_ != "ms"}
     if k.dsv4_device_status(clear=True) != 0:
         raise RuntimeError("device status error")
     peaks, src = measured_peaks()
     qbytes = w.T * w.H * (1024 + (1024 if bf16 else 512 + 4)) + w.T * (8 + 256)
     stages = {"quant": {"ms": ms_q, "bound": "hbm", "algorithmic": qbytes,
                         "achieved": qbytes / (ms_q * 1e-3) / 1e9, "unit": "GB/s",
-                        "peak": peaks["hbm_gbs"]}}
+                        "peak": peaks["hbm_gbs"], **spread(t_q)}}
     if gemm:
         fl = 2.0 * w.T * w.n_groups * w.o_lora_rank * w.D
         by = (w.n_groups * w.o_lora_rank * w.D + w.n_groups * w.T * w.D) * esz + \
@@ -532,11 +591,11 @@ def run_workload(args, ws, rank, local):
         if w.name == "decode":      # weight-read bound: bytes against HBM
             stages["wo_a"] = {"ms": ms_a, "bound": "hbm", "algorithmic": by,
                               "achieved": by / (ms_a * 1e-3) / 1e9, "unit": "GB/s",
-                              "peak": peaks["hbm_gbs"]}
+                              "peak": peaks["hbm_gbs"], **spread(t_a)}
         else:
             stages["wo_a"] = {"ms": ms_a, "bound": "tensor", "algorithmic": fl,
                               "achieved": fl / (ms_a * 1e-3) / 1e12, "unit": "TFLOP/s",
-                              "peak": tensor_peak}
+                              "peak": tensor_peak, **spread(t_a)}
     for s_ in stages.values():
         s_["frac"] = s_["achieved"] / s_["peak"]
     dom = max(stages, key=lambda n: stages[n]["ms"])
@@ -553,13 +612,14 @@ def run_workload(args, ws, rank, local):
                                (f", o_lora_rank {w.o_lora_rank}, " + ("bf16 inverse RoPE + bf16 "
                                 "grouped wo_a" if bf16 else "quant + grouped wo_a")
                                 if gemm else ", quantiser alone"),
-                   "timing": "CUDA-graph replay", "input_sets": nsets,
+                   "timing": "CUDA-graph replay, graphs of 10 calls; p10/p50/p90 over the "
+                             "replays", "input_sets": nsets,
                    "l2": f"{nsets} rotating input sets of {set_bytes / 1e6:.1f} MB (>= 3x L2)"},
         "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,
         "roofline": {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
                      "peak": ds["peak"], "unit": ds["unit"], "frac": ds["frac"],
                      "traffic": None, "peak_source": src},
-        "stages": stages,
+        "stages": stages, "step_spread": spread(t_step),
     }
     return result
 

@@ -48,6 +48,7 @@ def _load():
         I64 = ctypes.c_int64
         sig = {
             "oracle_num_threads": (ctypes.c_int, []),
+            "oracle_set_num_threads": (None, [ctypes.c_int]),
             "oracle_bf16_to_float": (ctypes.c_float, [ctypes.c_uint16]),
             "oracle_bf16_from_double": (ctypes.c_uint16, [ctypes.c_double]),
             "oracle_e4m3_decode": (ctypes.c_double, [ctypes.c_uint8]),
@@ -108,6 +109,11 @@ def _check(rc: int, what: str):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Thread count of the oracle's parallel loops (results do not depend on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 # -- number formats -------------------------------------------------------------

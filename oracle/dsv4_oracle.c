@@ -63,6 +63,18 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Sets the thread count of the parallel loops (timing only: every result is
+ * the same at any thread count, each output element being computed whole by
+ * one thread). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------ */
 /* Number formats                                                            */
 /* ------------------------------------------------------------------------ */

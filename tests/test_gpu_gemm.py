@@ -158,6 +158,18 @@ def test_o_proj_full_config_sampled(dev):
     assert np.array_equal(og, og2), "two runs differ"
 
 
+@pytest.mark.parametrize("name,T", [("decode", 64), ("decode", 7), ("full", 300)])
+def test_o_proj_deterministic(dev, name, T):
+    """Two runs of the whole chain give bit-identical output: decode shapes take
+    the split-K cluster path (partials added in a fixed order) with the 64-row
+    A box, T = 300 the programmatically launched GEMMs."""
+    w = di.WORKLOADS[name].with_tokens(T, seed=T + 11)
+    d = di.make_inputs(w)
+    og = _o_proj_gpu(d, w, dev)
+    og2 = _o_proj_gpu(d, w, dev)
+    assert np.array_equal(og, og2), "two runs differ"
+
+
 def test_o_proj_errors(dev):
     import deepseek_v4_attention_gb300 as k
     lib = k.load_library()
