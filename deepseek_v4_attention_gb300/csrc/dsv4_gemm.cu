@@ -11,18 +11,22 @@
 // or 256, see Cfg):
 //   warp 0, lane 0   TMA producer: A tile (128 tokens x 128 k) and B tile
 //                    (kBN rows x 128 k), both with the 128-byte swizzle.
-//   warp 1, lane 0   MMA issuer: four tcgen05.mma (K = 32) per k-block from
-//                    precomputed descriptors, one commit per stage; once per 4
-//                    k-blocks (one packed int32 of scales) tcgen05.cp of a
-//                    staged scale-factor slot into TMEM.
-//   warp 2           scale-factor warp: loads the A scale words of a pack with
-//                    coalesced loads and stores them in the 32 x 16-byte order
-//                    tcgen05.cp.32x128b.warpx4 expects (TMEM column c of lane
-//                    r = row 32 c + r); expands the raw 128 x 128 UE8M0 weight
-//                    bytes into the kBN-row B tile; ring of kSfSlots slots
-//                    guarded by sf_full / sf_empty barriers (sf_empty is
-//                    committed after the last MMA reading the slot, so it also
-//                    guards the slot's TMEM columns).
+//   warp 1, lane 0   MMA issuer: per k-block, tcgen05.cp of the stage's scale
+//                    factors into the stage's TMEM columns, then four
+//                    tcgen05.mma (K = 32) from precomputed descriptors, then
+//                    one commit that frees the stage.
+//   warp 2           scale-factor warp: each stage has its own scale-factor
+//                    slot, filled for the stage's k-block and completed on the
+//                    stage's full barrier (which therefore counts two
+//                    arrivals: the producer's and this warp's).  It loads the
+//                    A scale words of a pack (one packed int32 per row) with
+//                    coalesced loads, one pack ahead, and stores them in the
+//                    32 x 16-byte order tcgen05.cp.32x128b.warpx4 expects
+//                    (TMEM column c of lane r = row 32 c + r); it expands the
+//                    raw 128 x 128 UE8M0 weight bytes into the kBN-row B
+//                    scales.  The stage's empty barrier (committed after the
+//                    MMAs that read the stage) guards both the slot and its
+//                    TMEM columns.
 //   warps 3..        epilogue: per warp a 32-row x 128-column slice of the fp32
 //                    accumulator to registers (tcgen05.ld), release of the
 //                    accumulator, then bf16 conversion or the fused per-128
@@ -71,7 +75,7 @@ struct Cfg {
   static constexpr int kEpiWarp0 = 3;
   static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
   static constexpr uint32_t kBBytes = kBN * kBK;
-  static constexpr int kSfSlots = 4;
+  static constexpr int kSfSlots = kStages;   // one scale-factor slot per stage
   static constexpr uint32_t kSfbBytes = kBN * 4;
   static constexpr uint32_t kSfSlotBytes = kSfaBytes + kSfbBytes;
   static constexpr int kSfCol0 = kAccBufs * kBN;              // after the accumulators
@@ -85,8 +89,8 @@ struct Cfg {
   static constexpr uint32_t kEpiBufBytes = 2048;
   static constexpr uint32_t epi = (sf + kSfSlots * kSfSlotBytes + 1023) / 1024 * 1024;
   static constexpr uint32_t bars = epi + kEpiWarps * kEpiBufBytes;
-  // full/empty[kStages], tmem_full/empty[kAccBufs], sf_full/empty[kSfSlots], drain
-  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 2 * kSfSlots + 1;
+  // full/empty[kStages], tmem_full/empty[kAccBufs], drain
+  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 1;
   static constexpr uint32_t misc = bars + n_bars * 8;  // tmem base, abort flag
   static constexpr uint32_t total = misc + 16;
   static constexpr uint32_t smem_bytes = total + 1024;  // + alignment slack
@@ -176,9 +180,7 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* tmem_full = empty + kStages;
   uint64_t* tmem_empty = tmem_full + kAccBufs;
-  uint64_t* sf_full = tmem_empty + kAccBufs;
-  uint64_t* sf_empty = sf_full + C::kSfSlots;
-  uint64_t* drain = sf_empty + C::kSfSlots;
+  uint64_t* drain = tmem_empty + kAccBufs;
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::misc + 4);
 
@@ -189,16 +191,12 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], kBf16 ? 1 : 2);   // the producer's expect_tx (+ the scale-factor warp)
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < kAccBufs; ++a) {
       mbar_init(&tmem_full[a], 1);
       mbar_init(&tmem_empty[a], C::kEpiWarps);
-    }
-    for (int i = 0; i < C::kSfSlots; ++i) {
-      mbar_init(&sf_full[i], 1);
-      mbar_init(&sf_empty[i], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -287,26 +285,20 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      uint32_t packs_done = 0;  // scale-factor packs consumed so far (all tiles)
       bool ok = true;
       for (int tile = first_tile<kSplit>(); tile < p.num_tiles && ok;
            tile += tile_stride<kSplit>(p)) {
         if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        uint32_t sf_col = 0;
-        int slot = 0;
         for (int kb = kb_begin<kSplit>(p); kb < kb_end<kSplit>(p); ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          if (!kBf16 && (kb & 3) == 0) {
-            slot = static_cast<int>(packs_done % C::kSfSlots);
-            const uint32_t sp = (packs_done / C::kSfSlots) & 1u;
-            ++packs_done;
-            if (!mbar_wait(&sf_full[slot], sp, abort_flag, p.status)) { ok = false; break; }
-            tc_fence_after();
-            sf_col = tmem_base + static_cast<uint32_t>(C::kSfCol0 + slot * C::kSfColsPerSlot);
-            const uint64_t sd = sfdesc0 + ((slot * C::kSfSlotBytes) >> 4);
+          // the stage's scale factors arrived with its operands (same barrier)
+          const uint32_t sf_col =
+              tmem_base + static_cast<uint32_t>(C::kSfCol0 + stage * C::kSfColsPerSlot);
+          if (!kBf16) {
+            const uint64_t sd = sfdesc0 + ((stage * C::kSfSlotBytes) >> 4);
             tmem_cp_32x128b_x4(sf_col, sd);                     // A: the slot's first 512 B
 #pragma unroll
             for (int r = 0; r < kBN / 128; ++r)                 // B: 512 B per 128 rows
@@ -327,9 +319,7 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
               mma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, id, sf_col, sf_col + 4,
                        ((kb - kb_begin<kSplit>(p)) | k) != 0 ? 1u : 0u);
           }
-          mma_commit(&empty[stage]);
-          // the last k-block that reads this scale-factor slot releases it
-          if (!kBf16 && ((kb & 3) == 3 || kb == kb_end<kSplit>(p) - 1)) mma_commit(&sf_empty[slot]);
+          mma_commit(&empty[stage]);   // frees the stage's operands and scale-factor slot
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -362,7 +352,8 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
           if (lane + 32 * i < packs) wnext[r][i] = b_scale_word(p, rb + r, lane + 32 * i);
     }
     griddep_wait();  // the A scale words are written by the previous kernel
-    uint32_t n = 0;  // packs staged so far (all tiles)
+    int stage = 0;
+    uint32_t phase = 0;
     bool ok = true;
     for (int tile = first_tile<kSplit>(); tile < p.num_tiles && ok;
          tile += tile_stride<kSplit>(p)) {
@@ -385,31 +376,42 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
             wnext[r][i] = (lane + 32 * i < packs) ? b_scale_word(p, rb2 + r, lane + 32 * i) : 0u;
       }
       const int64_t m0 = static_cast<int64_t>(m_blk) * kBM;
-      for (int j = kb_begin<kSplit>(p) / 4; j < (kb_end<kSplit>(p) + 3) / 4; ++j) {
-        // the 128 scale words of this pack: lane r takes rows r, r+32, r+64, r+96
+      // the 128 A scale words of pack j: lane r takes rows r, r+32, r+64, r+96
+      auto load_pack = [&](int j, uint32_t (&v)[4]) {
         const int32_t* src = p.a_scale + (static_cast<int64_t>(g) * packs + j) * p.t_al + m0;
-        uint32_t v[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int64_t t = m0 + 32 * c + lane;
-          v[c] = t < p.T ? static_cast<uint32_t>(__ldg(src + 32 * c + lane)) : 0u;
+          v[c] = (j < packs && t < p.T) ? static_cast<uint32_t>(__ldg(src + 32 * c + lane)) : 0u;
         }
-        const int slot = static_cast<int>(n % C::kSfSlots);
-        const uint32_t sp = (n / C::kSfSlots) & 1u;
-        ++n;
-        if (!mbar_wait_warp(&sf_empty[slot], sp ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        uint4* dst = reinterpret_cast<uint4*>(smem + C::sf + slot * C::kSfSlotBytes);
-        dst[lane] = make_uint4(v[0], v[1], v[2], v[3]);
+      };
+      const int kb0 = kb_begin<kSplit>(p);
+      uint32_t vcur[4], vnext[4];
+      load_pack(kb0 / 4, vnext);
+      uint32_t bword[kRb];
+      for (int kb = kb0; kb < kb_end<kSplit>(p); ++kb) {
+        if (kb == kb0 || (kb & 3) == 0) {   // a new pack: its words, and the next pack's load
+          const int j = kb / 4;
 #pragma unroll
-        for (int r = 0; r < kRb; ++r) {
-          const uint32_t src_w = (j < 32) ? wcur[r][0] : (j < 64) ? wcur[r][1]
-                               : (j < 96) ? wcur[r][2] : wcur[r][3];
-          const uint32_t word = __shfl_sync(0xFFFFFFFFu, src_w, j & 31);
-          dst[32 + 32 * r + lane] = make_uint4(word, word, word, word);
+          for (int c = 0; c < 4; ++c) vcur[c] = vnext[c];
+          load_pack(j + 1, vnext);
+#pragma unroll
+          for (int r = 0; r < kRb; ++r) {
+            const uint32_t src_w = (j < 32) ? wcur[r][0] : (j < 64) ? wcur[r][1]
+                                 : (j < 96) ? wcur[r][2] : wcur[r][3];
+            bword[r] = __shfl_sync(0xFFFFFFFFu, src_w, j & 31);
+          }
         }
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        uint4* dst = reinterpret_cast<uint4*>(smem + C::sf + stage * C::kSfSlotBytes);
+        dst[lane] = make_uint4(vcur[0], vcur[1], vcur[2], vcur[3]);
+#pragma unroll
+        for (int r = 0; r < kRb; ++r)
+          dst[32 + 32 * r + lane] = make_uint4(bword[r], bword[r], bword[r], bword[r]);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sf_full[slot]);
+        if (lane == 0) mbar_arrive(&full[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
   } else if (warp >= C::kEpiWarp0) {
