@@ -54,6 +54,8 @@ def load_library() -> ctypes.CDLL:
     lib.dsv4_inv_rope_fp8_quant.argtypes = [P, P, P, I64, I64, I, I, I, I, I, P, P, P]
     lib.dsv4_inv_rope_fp8_quant.restype = I
     lib.dsv4_grouped_wo_a.argtypes = [P, P, I64, I, I, I, P, P, P, P]
+    lib.dsv4_inv_rope_grouped_wo_a.argtypes = [P, P, P, I64, I64, I, I, I, I, I, I, P, P, P, P]
+    lib.dsv4_inv_rope_grouped_wo_a.restype = I
     lib.dsv4_grouped_wo_a.restype = I
     lib.dsv4_o_proj_workspace_bytes.argtypes = [I64, I, I, I, I]
     lib.dsv4_o_proj_workspace_bytes.restype = ctypes.c_size_t
@@ -179,6 +181,50 @@ def dsv4_grouped_wo_a(x_fp8: torch.Tensor, x_scale: torch.Tensor, w_fp8: torch.T
     rc = lib.dsv4_grouped_wo_a(x_fp8.data_ptr(), x_scale.data_ptr(), T, G, D, o_lora_rank,
                                w_fp8.data_ptr(), w_scale.data_ptr(), z.data_ptr(), _stream(stream))
     _check(rc, "dsv4_grouped_wo_a")
+    return z
+
+
+FUSED_MAX_TOKENS = 64   # DSV4_FUSED_MAX_TOKENS
+
+
+def dsv4_inv_rope_grouped_wo_a(o: torch.Tensor, positions: torch.Tensor,
+                               cos_sin_cache: torch.Tensor, w_fp8: torch.Tensor,
+                               w_scale: torch.Tensor, n_groups: int, heads_per_group: int,
+                               o_lora_rank: int, nope_dim: int = 448, rope_dim: int = 64,
+                               quant_group_size: int = 128, *, z: torch.Tensor | None = None,
+                               stream=None) -> torch.Tensor:
+    """Quantiser fused into the grouped wo_a (decode sizes, T <= FUSED_MAX_TOKENS):
+    o [T, H, 512] bf16 -> z [T, G, R] bf16, equal to dsv4_grouped_wo_a of
+    dsv4_inv_rope_fp8_quant's output."""
+    lib = load_library()
+    _cuda(o, "o", torch.bfloat16)
+    _cuda(positions, "positions", torch.int64)
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    _cuda(w_fp8, "w_fp8", _FP8)
+    _cuda(w_scale, "w_scale", _SCALE8)
+    if o.dim() != 3 or not o.is_contiguous():
+        raise ValueError("o must be a contiguous [T, H, head_dim] tensor")
+    if not positions.is_contiguous() or not cos_sin_cache.is_contiguous():
+        raise ValueError("positions and cos_sin_cache must be contiguous")
+    T, H, hd = o.shape
+    if H != n_groups * heads_per_group or hd != nope_dim + rope_dim:
+        raise DSV4Error(-1, "dsv4_inv_rope_grouped_wo_a (o shape)")
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != rope_dim or positions.numel() != T:
+        raise DSV4Error(-1, "dsv4_inv_rope_grouped_wo_a (cache / positions shape)")
+    D = heads_per_group * hd
+    if tuple(w_fp8.shape) != (n_groups * o_lora_rank, D) or not w_fp8.is_contiguous():
+        raise ValueError("w_fp8 must be a contiguous [G*R, D] tensor")
+    if tuple(w_scale.shape) != (n_groups * o_lora_rank // 128, D // 128) or \
+            not w_scale.is_contiguous():
+        raise ValueError("w_scale must be a contiguous [G*R/128, D/128] tensor")
+    if z is None:
+        z = torch.empty((T, n_groups, o_lora_rank), dtype=torch.bfloat16, device=o.device)
+    rc = lib.dsv4_inv_rope_grouped_wo_a(o.data_ptr(), positions.data_ptr(),
+                                        cos_sin_cache.data_ptr(), T, cos_sin_cache.shape[0],
+                                        n_groups, heads_per_group, nope_dim, rope_dim,
+                                        quant_group_size, o_lora_rank, w_fp8.data_ptr(),
+                                        w_scale.data_ptr(), z.data_ptr(), _stream(stream))
+    _check(rc, "dsv4_inv_rope_grouped_wo_a")
     return z
 
 

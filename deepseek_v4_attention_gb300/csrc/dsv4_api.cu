@@ -184,6 +184,46 @@ int dsv4_grouped_wo_a(const void* x_fp8, const int32_t* x_scale, int64_t num_tok
   return rc;
 }
 
+int dsv4_inv_rope_grouped_wo_a(const void* o, const int64_t* positions,
+                               const float* cos_sin_cache, int64_t num_tokens, int64_t max_pos,
+                               int n_groups, int heads_per_group, int nope_dim, int rope_dim,
+                               int quant_group_size, int o_lora_rank, const void* w_fp8,
+                               const uint8_t* w_scale, void* z, void* stream) {
+  t_last_launches = 0;
+  int rc = check_quant_shapes(num_tokens, max_pos, n_groups, heads_per_group, nope_dim, rope_dim,
+                              quant_group_size);
+  if (rc != DSV4_OK) return rc;
+  if (o_lora_rank <= 0 || o_lora_rank % 128 != 0) return DSV4_ERR_SHAPE;
+  if ((rc = check_quant_supported(nope_dim, rope_dim, quant_group_size)) != DSV4_OK) return rc;
+  if (num_tokens == 0) return DSV4_OK;
+  if (num_tokens > DSV4_FUSED_MAX_TOKENS || max_pos > INT32_MAX) return DSV4_ERR_UNSUPPORTED;
+  if (!o || !positions || !cos_sin_cache || !w_fp8 || !w_scale || !z) return DSV4_ERR_NULL;
+  if (!aligned16(o) || !aligned16(positions) || !aligned16(cos_sin_cache) || !aligned16(w_fp8) ||
+      !aligned16(z))
+    return DSV4_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = get_device_info(&dev)) != DSV4_OK) return rc;
+  GemmProblem p;
+  p.T = num_tokens;
+  p.G = n_groups;
+  p.N = o_lora_rank;
+  p.K = heads_per_group * (nope_dim + rope_dim);
+  p.b = w_fp8;
+  p.b_scale = w_scale;
+  p.epilogue = kEpiBf16;
+  p.out_bf16 = z;
+  p.fused_a = true;
+  p.o = static_cast<const uint16_t*>(o);
+  p.positions = positions;
+  p.cache = cos_sin_cache;
+  p.max_pos = max_pos;
+  p.heads = n_groups * heads_per_group;
+  p.heads_per_group = heads_per_group;
+  rc = launch_block_scaled_gemm(p, static_cast<cudaStream_t>(stream), dev);
+  if (rc == DSV4_OK) t_last_launches = 1;
+  return rc;
+}
+
 int dsv4_inv_rope_bf16(const void* o, const int64_t* positions, const float* cos_sin_cache,
                        int64_t num_tokens, int64_t max_pos, int n_groups, int heads_per_group,
                        int nope_dim, int rope_dim, void* out_bf16, void* stream) {

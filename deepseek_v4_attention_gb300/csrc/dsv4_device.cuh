@@ -103,6 +103,31 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
   return __all_sync(0xFFFFFFFFu, done);
 }
 
+// Warp-uniform wait for roles that wait long and must not take issue slots
+// from compute warps on the same scheduler: only lane 0 polls, sleeping
+// `sleep_ns` between polls; the other lanes wait at the warp barrier.  Same
+// time limit and abort rules as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_warp_lazy(uint64_t* bar, uint32_t parity,
+                                                    volatile int* abort_flag, int* status,
+                                                    unsigned sleep_ns) {
+  int done = 1;
+  if ((threadIdx.x & 31) == 0 && !mbar_try_wait(bar, parity)) {
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      __nanosleep(sleep_ns);
+      if (mbar_try_wait(bar, parity)) break;
+      if (*abort_flag) { done = 0; break; }
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        record_status(status, DSV4_ERR_TIMEOUT);
+        done = 0;
+        break;
+      }
+    }
+  }
+  return __shfl_sync(0xFFFFFFFFu, done, 0) != 0;
+}
+
 // A shorter wait used only while draining after an abort.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
@@ -201,6 +226,38 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
 // cluster arrives once); release/acquire order shared::cluster accesses.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// ------------------------------------------------- quantisation helpers --
+// Shared by the quantiser and the GEMM's fused producer warps, so that both
+// produce the same codes and scales bit for bit.
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// Inverse rotation of one interleaved pair (a, b) by the angle with cosine c
+// and sine s, in fp32 with a fixed order: each cross product is rounded first.
+__device__ __forceinline__ void inv_rotate(float& a, float& b, float c, float s) {
+  const float bs = __fmul_rn(b, s);
+  const float as = __fmul_rn(a, s);
+  const float y0 = __fmaf_rn(a, c, bs);
+  const float y1 = __fmaf_rn(b, c, -as);
+  a = y0;
+  b = y1;
+}
+
+// Maximum over the 16 lanes of a half-warp.
+__device__ __forceinline__ float half_warp_max(float v) {
+#pragma unroll
+  for (int m = 8; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+  return v;
 }
 
 // ---------------------------------------------------------------- tcgen05 --
@@ -353,6 +410,16 @@ __device__ __forceinline__ float exp2_neg(int e) {
 __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   return static_cast<uint16_t>(
       __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Quantises 8 values with scale 2^e (inv_scale = 2^-e) into 8 e4m3 bytes.
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float inv_scale) {
+  uint2 r;
+  r.x = static_cast<uint32_t>(e4m3x2(f[0] * inv_scale, f[1] * inv_scale)) |
+        (static_cast<uint32_t>(e4m3x2(f[2] * inv_scale, f[3] * inv_scale)) << 16);
+  r.y = static_cast<uint32_t>(e4m3x2(f[4] * inv_scale, f[5] * inv_scale)) |
+        (static_cast<uint32_t>(e4m3x2(f[6] * inv_scale, f[7] * inv_scale)) << 16);
+  return r;
 }
 
 }  // namespace dsv4

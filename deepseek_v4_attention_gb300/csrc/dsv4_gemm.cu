@@ -42,6 +42,8 @@
 // scaled by the same power of two.  The byte is chosen with the
 // scale-factor-id field of the instruction descriptor: the 4 blocks of a
 // packed int32 are bytes 0..3 of one TMEM column word.
+#include <string.h>
+
 #include "dsv4_device.cuh"
 #include "dsv4_internal.h"
 
@@ -66,14 +68,18 @@ constexpr uint32_t kSfaBytes = kBM * 4;    // 512 B
 // 64 rows (the next bytes of shared memory) only reach accumulator rows that
 // are never stored.  The smaller stage fits 8 stages instead of 6, a third more
 // weight bytes in flight per CTA.
-template <int kBN, int kARows = 128>
+template <int kBN, int kARows = 128, bool kFused = false>
 struct Cfg {
   static constexpr uint32_t kABytes = kARows * kBK;
-  static constexpr int kStages = (kARows == 64) ? 8 : (kBN == 128) ? 6 : 4;
+  static constexpr int kStages = kFused ? 6 : (kARows == 64) ? 8 : (kBN == 128) ? 6 : 4;
   static constexpr int kAccBufs = (kBN == 128) ? 2 : 1;
   static constexpr int kEpiWarps = (kBN == 128) ? 4 : 8;
   static constexpr int kEpiWarp0 = 3;
-  static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+  // fused A (kFused): four producer warps after the epilogue warps build the
+  // A tile from the attention output (16 token rows each)
+  static constexpr int kProdWarps = kFused ? 4 : 0;
+  static constexpr int kProdWarp0 = kEpiWarp0 + kEpiWarps;
+  static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + kProdWarps);
   static constexpr uint32_t kBBytes = kBN * kBK;
   static constexpr int kSfSlots = kStages;   // one scale-factor slot per stage
   static constexpr uint32_t kSfbBytes = kBN * 4;
@@ -85,12 +91,18 @@ struct Cfg {
   static constexpr uint32_t a = 0;
   static constexpr uint32_t b = a + kStages * kABytes;
   static constexpr uint32_t sf = b + kStages * kBBytes;
+  // fused A: a ring of kOStages bf16 slices of the attention output (kARows
+  // token rows x 128 elements of one head, 256 B a row), loaded by TMA ahead
+  // of the producer warps
+  static constexpr int kOStages = kFused ? 3 : 0;
+  static constexpr uint32_t kOBytes = kARows * 256;
+  static constexpr uint32_t ostage = (sf + kSfSlots * kSfSlotBytes + 1023) / 1024 * 1024;
   // per epilogue warp, a 2 KiB staging buffer for its TMA stores (32 rows x 64 B)
   static constexpr uint32_t kEpiBufBytes = 2048;
-  static constexpr uint32_t epi = (sf + kSfSlots * kSfSlotBytes + 1023) / 1024 * 1024;
+  static constexpr uint32_t epi = ostage + kOStages * kOBytes;
   static constexpr uint32_t bars = epi + kEpiWarps * kEpiBufBytes;
-  // full/empty[kStages], tmem_full/empty[kAccBufs], drain
-  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 1;
+  // full/empty[kStages], tmem_full/empty[kAccBufs], drain, o_full/o_empty[kOStages]
+  static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 1 + 2 * kOStages;
   static constexpr uint32_t misc = bars + n_bars * 8;  // tmem base, abort flag
   static constexpr uint32_t total = misc + 16;
   static constexpr uint32_t smem_bytes = total + 1024;  // + alignment slack
@@ -108,6 +120,12 @@ struct Params {
   uint8_t* q_out;          // [T][G*N]
   int32_t* q_scale;        // [ceil(G*N/512)][t_al]
   int* status;             // device status word
+  // fused A only
+  const uint16_t* o;       // bf16 [T][H][512]
+  const int64_t* positions;
+  const float* cache;      // fp32 [max_pos][64]
+  int64_t max_pos;
+  int H, hpg;
 };
 
 __device__ __forceinline__ void tile_coords(const Params& p, int tile, int& g, int& n_blk,
@@ -158,12 +176,13 @@ __device__ __forceinline__ int kb_end(const Params& p) {
   return kSplit > 1 ? kb_begin<kSplit>(p) + p.k_blocks / kSplit : p.k_blocks;
 }
 
-template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows>
-__global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
+template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows, bool kFused>
+__global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b,
                              const __grid_constant__ CUtensorMap tm_out, const Params p) {
-  using C = Cfg<kBN, kARows>;
+  using C = Cfg<kBN, kARows, kFused>;
+  static_assert(!kFused || (!kBf16 && kARows == 64 && kBN == 128), "fused A: decode tiles");
   constexpr uint32_t kABytes = C::kABytes;
   constexpr int kStages = C::kStages;
   constexpr int kAccBufs = C::kAccBufs;
@@ -181,6 +200,8 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
   uint64_t* tmem_full = empty + kStages;
   uint64_t* tmem_empty = tmem_full + kAccBufs;
   uint64_t* drain = tmem_empty + kAccBufs;
+  uint64_t* o_full = drain + 1;               // fused A: the attention-output ring
+  uint64_t* o_empty = o_full + C::kOStages;
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::misc + 4);
 
@@ -191,7 +212,8 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], kBf16 ? 1 : 2);   // the producer's expect_tx (+ the scale-factor warp)
+      // the producer's expect_tx, the scale-factor warp (FP8), the A producers (fused)
+      mbar_init(&full[s], kBf16 ? 1 : 2 + C::kProdWarps);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < kAccBufs; ++a) {
@@ -199,11 +221,15 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
       mbar_init(&tmem_empty[a], C::kEpiWarps);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < C::kOStages; ++i) {
+      mbar_init(&o_full[i], 1);               // the TMA thread's expect_tx
+      mbar_init(&o_empty[i], C::kProdWarps);  // every producer warp has read it
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_a);
+    if constexpr (!kFused) tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
     tma_prefetch_desc(&tm_out);
   }
@@ -222,6 +248,8 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // bit s: stage s loaded / parity of its phase
+      int oj = 0;                              // fused A: the o ring
+      uint32_t ophase = 0, o_issued = 0, o_issued_parity = 0;
       bool ok = true;
       // Before the previous kernel of the stream has finished (programmatic
       // launch) only the weights may be read: the first stages of the first
@@ -234,7 +262,8 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
         const int kbs = kb_end<kSplit>(p) - kb_begin<kSplit>(p);
         early = kbs < kStages ? kbs : kStages;
         for (int i = 0; i < early; ++i) {
-          mbar_arrive_expect_tx(&full[i], kABytes + kBBytes);
+          // fused A: the producer warps write A; only B travels by TMA
+          mbar_arrive_expect_tx(&full[i], kFused ? kBBytes : kABytes + kBBytes);
           tma_load_2d(smem + C::b + i * kBBytes, &tm_b, &full[i],
                       (kb_begin<kSplit>(p) + i) * kBKe, brow);
         }
@@ -244,11 +273,23 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
            tile += tile_stride<kSplit>(p)) {
         int g, n_blk, m_blk;
         tile_coords(p, tile, g, n_blk, m_blk);
-        const int m0 = m_blk * kBM;
+        [[maybe_unused]] const int m0 = m_blk * kBM;
         const int brow = g * p.N + n_blk * kBN;
         for (int kb = kb_begin<kSplit>(p); kb < kb_end<kSplit>(p); ++kb) {
+          if constexpr (kFused) {
+            // this k-block's slice of o: rows m0.., head g*hpg + kb/4, elements
+            // (kb % 4)*128 .. +127 (rows past T zero-filled)
+            if (!mbar_wait(&o_empty[oj], ophase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            mbar_arrive_expect_tx(&o_full[oj], C::kOBytes);
+            tma_load_2d(smem + C::ostage + oj * C::kOBytes, &tm_a, &o_full[oj],
+                        (g * p.hpg + (kb >> 2)) * 512 + (kb & 3) * 128, m0);
+            o_issued |= 1u << oj;
+            o_issued_parity = (o_issued_parity & ~(1u << oj)) | (ophase << oj);
+            if (++oj == C::kOStages) { oj = 0; ophase ^= 1u; }
+          }
           if (early > 0) {  // B already in flight for this stage
-            tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBKe, m0, g);
+            if constexpr (!kFused)
+              tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBKe, m0, g);
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -256,8 +297,9 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
             continue;
           }
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
-          tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBKe, m0, g);
+          mbar_arrive_expect_tx(&full[stage], kFused ? kBBytes : kABytes + kBBytes);
+          if constexpr (!kFused)
+            tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBKe, m0, g);
           tma_load_2d(smem + C::b + stage * kBBytes, &tm_b, &full[stage], kb * kBKe, brow);
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -268,6 +310,8 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
         // drain: let every copy issued here land before the CTA exits
         for (int s = 0; s < kStages; ++s)
           if (issued & (1u << s)) mbar_wait_drain(&full[s], (issued_parity >> s) & 1u);
+        for (int s = 0; s < C::kOStages; ++s)
+          if (o_issued & (1u << s)) mbar_wait_drain(&o_full[s], (o_issued_parity >> s) & 1u);
       }
     }
   } else if (warp == 1) {
@@ -386,15 +430,17 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
         }
       };
       const int kb0 = kb_begin<kSplit>(p);
-      uint32_t vcur[4], vnext[4];
-      load_pack(kb0 / 4, vnext);
+      uint32_t vcur[4] = {0u, 0u, 0u, 0u}, vnext[4] = {0u, 0u, 0u, 0u};
+      if constexpr (!kFused) load_pack(kb0 / 4, vnext);   // fused A: the producers write SFA
       uint32_t bword[kRb];
       for (int kb = kb0; kb < kb_end<kSplit>(p); ++kb) {
         if (kb == kb0 || (kb & 3) == 0) {   // a new pack: its words, and the next pack's load
           const int j = kb / 4;
+          if constexpr (!kFused) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) vcur[c] = vnext[c];
-          load_pack(j + 1, vnext);
+            for (int c = 0; c < 4; ++c) vcur[c] = vnext[c];
+            load_pack(j + 1, vnext);
+          }
 #pragma unroll
           for (int r = 0; r < kRb; ++r) {
             const uint32_t src_w = (j < 32) ? wcur[r][0] : (j < 64) ? wcur[r][1]
@@ -402,12 +448,124 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
             bword[r] = __shfl_sync(0xFFFFFFFFu, src_w, j & 31);
           }
         }
-        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        // fused A: the producer warps need the issue slots, so this warp sleeps
+        const bool got = kFused
+            ? mbar_wait_warp_lazy(&empty[stage], phase ^ 1u, abort_flag, p.status, 64)
+            : mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.status);
+        if (!got) { ok = false; break; }
         uint4* dst = reinterpret_cast<uint4*>(smem + C::sf + stage * C::kSfSlotBytes);
-        dst[lane] = make_uint4(vcur[0], vcur[1], vcur[2], vcur[3]);
+        if constexpr (!kFused) dst[lane] = make_uint4(vcur[0], vcur[1], vcur[2], vcur[3]);
 #pragma unroll
         for (int r = 0; r < kRb; ++r)
           dst[32 + 32 * r + lane] = make_uint4(bword[r], bword[r], bword[r], bword[r]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (kFused && warp >= C::kProdWarp0) {
+    // ---------------------------------------------- fused A producer (T <= 64)
+    // Builds each stage's A tile from the attention output: the inverse
+    // rotation, the per-128 block scale and the e4m3 cast of the quantiser
+    // (the same helpers, so the same codes and scales bit for bit), written in
+    // the 128-byte-swizzled layout the MMA reads (16-byte unit u of row r at
+    // u ^ (r & 7)), and each row's scale byte, as byte kb % 4 of its word in
+    // the stage's scale-factor slot.  The k-block's bf16 slice arrives by TMA
+    // in the o ring; a half-warp owns one token row (lane l16 holds its
+    // elements 8 l16 .. 8 l16 + 7, 16 contiguous bytes of the row's 256);
+    // warp pw owns rows 16 pw .. 16 pw + 15, two per step.  The cos/sin
+    // values of a row's rope lanes are loaded once per tile.
+    constexpr int kSteps = kARows / (2 * (C::kProdWarps > 0 ? C::kProdWarps : 1));
+    const int pw = warp - C::kProdWarp0;
+    const int half = lane >> 4;
+    const int l16 = lane & 15;
+    const bool rope_lane = l16 >= 8;     // block 3: head offsets 448 .. 511
+    const int quad = l16 - 8;            // rope pairs 4 quad .. 4 quad + 3
+    int stage = 0, oj = 0;
+    uint32_t phase = 0, ophase = 0;
+    bool ok = true;
+    for (int tile = first_tile<kSplit>(); tile < p.num_tiles && ok;
+         tile += tile_stride<kSplit>(p)) {
+      int g, n_blk, m_blk;
+      tile_coords(p, tile, g, n_blk, m_blk);
+      const int64_t m0 = static_cast<int64_t>(m_blk) * kBM;
+      // each row's position; one outside [0, max_pos) is recorded and leaves
+      // the row unrotated, as in the quantiser
+      bool rot[kSteps];
+      float4 cs[kSteps], sn[kSteps];
+#pragma unroll
+      for (int st = 0; st < kSteps; ++st) {
+        const int64_t t = m0 + 16 * pw + 2 * st + half;
+        rot[st] = false;
+        cs[st] = make_float4(0.f, 0.f, 0.f, 0.f);
+        sn[st] = cs[st];
+        if (t < p.T) {
+          const int64_t pos = __ldg(p.positions + t);
+          if (pos >= 0 && pos < p.max_pos) {
+            rot[st] = true;
+            if (rope_lane) {
+              const float4* row = reinterpret_cast<const float4*>(p.cache + pos * 64);
+              cs[st] = __ldg(row + quad);
+              sn[st] = __ldg(row + 8 + quad);
+            }
+          } else if (l16 == 0) {
+            record_status(p.status, DSV4_ERR_RANGE);
+          }
+        }
+      }
+      for (int kb = kb_begin<kSplit>(p); kb < kb_end<kSplit>(p); ++kb) {
+        const int qb = kb & 3;
+        if (!mbar_wait_warp(&o_full[oj], ophase, abort_flag, p.status)) { ok = false; break; }
+        const uint4* slice = reinterpret_cast<const uint4*>(smem + C::ostage + oj * C::kOBytes);
+        uint4 v[kSteps];
+#pragma unroll
+        for (int st = 0; st < kSteps; ++st) v[st] = slice[(16 * pw + 2 * st + half) * 16 + l16];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&o_empty[oj]);   // the slice is in registers
+        if (++oj == C::kOStages) { oj = 0; ophase ^= 1u; }
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        uint8_t* a_st = smem + C::a + stage * kABytes;
+        uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + C::sf + stage * C::kSfSlotBytes);
+        // The eight rows are independent: their maxima are reduced together
+        // (each shuffle level for all rows before the next), so the shuffle
+        // latencies overlap; the values are unpacked (and rotated) again for
+        // the cast instead of being held.
+        auto values = [&](int st, float (&f)[8]) {
+          unpack8(v[st], f);
+          if (qb == 3 && rope_lane && rot[st]) {
+            inv_rotate(f[0], f[1], cs[st].x, sn[st].x);
+            inv_rotate(f[2], f[3], cs[st].y, sn[st].y);
+            inv_rotate(f[4], f[5], cs[st].z, sn[st].z);
+            inv_rotate(f[6], f[7], cs[st].w, sn[st].w);
+          }
+        };
+        float m[kSteps];
+#pragma unroll
+        for (int st = 0; st < kSteps; ++st) {
+          float f[8];
+          values(st, f);
+          m[st] = 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) m[st] = fmaxf(m[st], fabsf(f[j]));
+        }
+#pragma unroll
+        for (int mask = 8; mask >= 1; mask >>= 1)
+#pragma unroll
+          for (int st = 0; st < kSteps; ++st)
+            m[st] = fmaxf(m[st], __shfl_xor_sync(0xFFFFFFFFu, m[st], mask));
+#pragma unroll
+        for (int st = 0; st < kSteps; ++st) {
+          float f[8];
+          values(st, f);
+          const int e = ue8m0_exponent(m[st]);
+          const uint2 q = quant8(f, exp2_neg(e));
+          const int r = 16 * pw + 2 * st + half;
+          *reinterpret_cast<uint2*>(a_st + r * 128 + ((((l16 >> 1) ^ (r & 7)) << 4) |
+                                                      ((l16 & 1) << 3))) = q;
+          // scale word of row r: lane r % 32, column r / 32 of the slot's A part
+          if (l16 == 0) sfa[(r & 31) * 4 + (r >> 5)] = static_cast<uint32_t>(e + 127) << (8 * qb);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[stage]);
@@ -427,7 +585,11 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
          tile += tile_stride<kSplit>(p)) {
       int g, n_blk, m_blk;
       tile_coords(p, tile, g, n_blk, m_blk);
-      if (!mbar_wait_warp(&tmem_full[acc], acc_phase, abort_flag, p.status)) break;
+      // fused A: the accumulator wait spans the mainloop; sleep instead of spinning
+      const bool got = kFused
+          ? mbar_wait_warp_lazy(&tmem_full[acc], acc_phase, abort_flag, p.status, 128)
+          : mbar_wait_warp(&tmem_full[acc], acc_phase, abort_flag, p.status);
+      if (!got) break;
       tc_fence_after();
       const int64_t t = static_cast<int64_t>(m_blk) * kBM + row;
       const bool live = t < p.T;
@@ -566,7 +728,9 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows>::kThreads, 1)
     }
   }
   if constexpr (kSplit > 1) {
-    if (warp < C::kEpiWarp0) {         // producer, MMA and scale-factor warps
+    // every thread of the cluster meets both barriers of the reduction:
+    // the producer, MMA and scale-factor warps (and the fused A producers) here
+    if (warp < C::kEpiWarp0 || (kFused && warp >= C::kProdWarp0)) {
       __syncwarp();                    // lane 0 of warps 0 and 1 finished its loop
       cluster_sync();
       cluster_sync();
@@ -612,16 +776,16 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows>
+template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows, bool kFused = false>
 int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
   // q.after_own_kernel: the previous kernel on the stream is one of this
   // library's (inside dsv4_o_proj), so the launch may overlap it: this kernel
   // reads only weights before griddep_wait().
-  using C = Cfg<kBN, kARows>;
+  using C = Cfg<kBN, kARows, kFused>;
   static int configured_for[64] = {0};
   if (dev.device < 0 || dev.device >= 64) return DSV4_ERR_UNSUPPORTED;
   if (!configured_for[dev.device]) {
-    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows>,
+    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows, kFused>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::smem_bytes)) != cudaSuccess)
       return DSV4_ERR_CUDA;
@@ -637,7 +801,17 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUtensorMap tm_a, tm_b;
-  {
+  if (kFused) {
+    // fused A: tm_a maps the attention output o as [T][H*512] bf16; a box is
+    // kARows token rows x 128 elements (one head's k-block), rows past T
+    // zero-filled
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(q.heads) * 512, static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(q.heads) * 512 * 2};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(kARows)};
+    if (!encode(&tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q.o, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+      return DSV4_ERR_CUDA;
+  } else {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(q.K), static_cast<cuuint64_t>(T),
                           static_cast<cuuint64_t>(q.G)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.K) * esz,
@@ -684,6 +858,12 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   p.q_out = q.q_out;
   p.q_scale = q.q_scale;
   p.status = dev.status;
+  p.o = q.o;
+  p.positions = q.positions;
+  p.cache = q.cache;
+  p.max_pos = q.max_pos;
+  p.H = q.heads;
+  p.hpg = q.heads_per_group;
 
   // persistent: one CTA per SM; split-K: one cluster of kSplit CTAs per tile
   const int grid = kSplit == 1 ? (p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms)
@@ -709,8 +889,8 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows>, tm_a,
-                         tm_b, tm_out, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows, kFused>,
+                         tm_a, tm_b, tm_out, p) != cudaSuccess)
     return DSV4_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
@@ -719,6 +899,21 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
 
 int launch_block_scaled_gemm(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
   if (q.K / 128 > 4 * 32 * 4) return DSV4_ERR_UNSUPPORTED;  // weight-scale words held per lane
+  if (q.fused_a) {
+    // decode sizes only: one 64-row m-tile, 128-wide tiles, split over K when
+    // both halves hold whole scale packs and the split still fits the GPU
+    if (q.bf16 || q.T > 64 || q.N % 128 != 0 || q.K != q.heads_per_group * 512)
+      return DSV4_ERR_UNSUPPORTED;
+    const int64_t tiles = static_cast<int64_t>(q.N / 128) * q.G;
+    const bool split = (q.K / 128) % 8 == 0 && 2 * tiles <= dev.num_sms;
+    const bool quant = q.epilogue == kEpiQuant;
+    if (split) {
+      if (quant) return launch_impl<128, kEpiQuant, 2, false, 64, true>(q, stream, dev);
+      return launch_impl<128, kEpiBf16, 2, false, 64, true>(q, stream, dev);
+    }
+    if (quant) return launch_impl<128, kEpiQuant, 1, false, 64, true>(q, stream, dev);
+    return launch_impl<128, kEpiBf16, 1, false, 64, true>(q, stream, dev);
+  }
   // 256-wide tiles when they divide N and still give every SM a tile;
   // otherwise 128-wide tiles (twice the CTAs, for the small decode shapes)
   const int64_t m_tiles = (q.T + kBM - 1) / kBM;

@@ -36,6 +36,17 @@ struct GemmProblem {
   bool bf16 = false;                // A and B bf16, no scales (kind::f16), K % 64 == 0
   bool after_own_kernel = false;    // previous kernel on the stream is this library's own:
                                     // launch with programmatic stream serialization
+  // Fused A (decode sizes, T <= 64): the kernel's producer warps build A from
+  // the attention output (inverse rotation + per-128 FP8 quantisation, the
+  // quantiser's arithmetic) instead of reading a pre-quantised a / a_scale;
+  // K = heads_per_group * 512.
+  bool fused_a = false;
+  const uint16_t* o = nullptr;      // bf16 [T][heads][512]
+  const int64_t* positions = nullptr;
+  const float* cache = nullptr;     // fp32 [max_pos][64], cos || sin
+  int64_t max_pos = 0;
+  int heads = 0;                    // G * heads_per_group
+  int heads_per_group = 0;
   void* out_bf16 = nullptr;         // bf16 [T][G*N] (kEpiBf16)
   uint8_t* q_out = nullptr;         // e4m3 [T][G*N]           (kEpiQuant)
   int32_t* q_scale = nullptr;       // int32 [ceil(G*N/512)][T_al] (kEpiQuant)

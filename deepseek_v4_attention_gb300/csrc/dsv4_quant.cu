@@ -31,41 +31,6 @@ namespace {
 constexpr int kHeadDim = 512;
 constexpr int kRope = 64;
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
-  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-}
-
-__device__ __forceinline__ void inv_rotate(float& a, float& b, float c, float s) {
-  const float bs = __fmul_rn(b, s);
-  const float as = __fmul_rn(a, s);
-  const float y0 = __fmaf_rn(a, c, bs);
-  const float y1 = __fmaf_rn(b, c, -as);
-  a = y0;
-  b = y1;
-}
-
-__device__ __forceinline__ float half_warp_max(float v) {
-#pragma unroll
-  for (int m = 8; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
-  return v;
-}
-
-// Quantises 8 values with scale 2^e into 8 e4m3 bytes.
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float inv_scale) {
-  uint2 r;
-  r.x = static_cast<uint32_t>(e4m3x2(f[0] * inv_scale, f[1] * inv_scale)) |
-        (static_cast<uint32_t>(e4m3x2(f[2] * inv_scale, f[3] * inv_scale)) << 16);
-  r.y = static_cast<uint32_t>(e4m3x2(f[4] * inv_scale, f[5] * inv_scale)) |
-        (static_cast<uint32_t>(e4m3x2(f[6] * inv_scale, f[7] * inv_scale)) << 16);
-  return r;
-}
-
 // One warp iteration = kU consecutive heads of one token (H % kU == 0): the
 // position and the cos/sin row are loaded once for the kU heads, and all 2*kU
 // 16-byte loads of o are issued before any value is used.

@@ -111,6 +111,40 @@ int dsv4_grouped_wo_a(const void* x_fp8, const int32_t* x_scale, int64_t num_tok
                       int n_groups, int group_dim, int o_lora_rank, const void* w_fp8,
                       const uint8_t* w_scale, void* z, void* stream);
 
+/* Largest token count the fused path below serves (decode sizes). */
+#define DSV4_FUSED_MAX_TOKENS 64
+
+/*
+ * Inverse RoPE + FP8 quantisation fused into the grouped wo_a projection, for
+ * decode sizes (num_tokens <= DSV4_FUSED_MAX_TOKENS).  The quantiser's work
+ * (dsv4_inv_rope_fp8_quant: the same rotation, scale rule and e4m3 cast, bit
+ * for bit) is done by producer warps of the GEMM kernel, which write the FP8
+ * A tile and its scales straight into shared memory; the FP8 activation never
+ * goes to device memory.  This is the fusion of the quantiser into the grouped
+ * GEMM that the o_proj page's fused_inv_rope_fp8_quant -> fp8_einsum sequence
+ * admits: z equals dsv4_grouped_wo_a applied to dsv4_inv_rope_fp8_quant's
+ * output on the same inputs.  Each CTA quantises the A rows of its own
+ * 128-column tile, so the quantiser's work is repeated once per column tile
+ * (R / 128 times); at the decode sizes measured this makes the one launch
+ * slower than the two separate ones, and dsv4_o_proj keeps the separate calls.
+ *
+ *   o, positions, cos_sin_cache, sizes: as dsv4_inv_rope_fp8_quant
+ *   o_lora_rank  R, a positive multiple of 128
+ *   w_fp8, w_scale, z: as dsv4_grouped_wo_a (z bf16 [T, G, R] contiguous)
+ *
+ * Errors: as dsv4_inv_rope_fp8_quant for the quantiser's arguments,
+ * DSV4_ERR_SHAPE for R, DSV4_ERR_UNSUPPORTED when num_tokens exceeds
+ * DSV4_FUSED_MAX_TOKENS or max_pos exceeds INT32_MAX (use the two separate
+ * calls), DSV4_ERR_NULL / DSV4_ERR_ALIGN (16 bytes) for pointers.  An
+ * out-of-range position sets DSV4_ERR_RANGE in the device status word, as in
+ * the quantiser.
+ */
+int dsv4_inv_rope_grouped_wo_a(const void* o, const int64_t* positions,
+                               const float* cos_sin_cache, int64_t num_tokens, int64_t max_pos,
+                               int n_groups, int heads_per_group, int nope_dim, int rope_dim,
+                               int quant_group_size, int o_lora_rank, const void* w_fp8,
+                               const uint8_t* w_scale, void* z, void* stream);
+
 /*
  * quantize=False variant of dsv4_inv_rope_fp8_quant: the bf16 inverse-rotated
  * groups (vLLM docs, grouped_wo_a, grouped_input: "The BF16 inverse-rotated
@@ -162,6 +196,7 @@ size_t dsv4_o_proj_workspace_bytes(int64_t num_tokens, int n_groups, int heads_p
  *     out[t, h] = bf16( sum_c zq[t,c] 2^ez[t,c/128] * Wb[h,c] 2^eb[h/128, c/128] ).
  * The activation quantisation inside wo_b is not printed on the pages; this
  * is its plainest reading (the same per-128 UE8M0 rule as wo_a's input).
+ * Three launches.
  *
  *   o, positions, cos_sin_cache, max_pos, sizes: as dsv4_inv_rope_fp8_quant
  *   wo_a_fp8, wo_a_scale : as dsv4_grouped_wo_a (w_fp8, w_scale)

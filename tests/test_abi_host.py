@@ -22,6 +22,7 @@ def test_exports_every_header_function(lib):
                           "dsv4_o_proj_workspace_bytes", "dsv4_o_proj", "dsv4_o_proj_with_events",
                           "dsv4_o_proj_static", "dsv4_selftest_wait_timeout",
                           "dsv4_inv_rope_bf16", "dsv4_grouped_wo_a_bf16",
+                          "dsv4_inv_rope_grouped_wo_a",
                           "dsv4_status_string",
                           "dsv4_device_status", "dsv4_last_launch_count"}
     out = subprocess.run(["nm", "-D", "--defined-only", k.LIB_PATH], capture_output=True,
@@ -72,6 +73,27 @@ def test_gemm_host_validation_without_gpu(lib):
     for idx in (0, 1, 6, 8):
         a = list(good); a[idx] = P + 8
         assert f(*a) == -3
+
+
+def test_fused_wo_a_host_validation_without_gpu(lib):
+    """dsv4_inv_rope_grouped_wo_a: the quantiser's asserts, R, the decode-size
+    limit (DSV4_FUSED_MAX_TOKENS = 64) and max_pos < 2^31, then pointers."""
+    f = lib.dsv4_inv_rope_grouped_wo_a
+    P = 4096
+    good = [P, P, P, 16, 4096, 2, 2, 448, 64, 128, 128, P, P, P, None]
+    for idx, val, rc in [(3, -1, -1), (4, 0, -1), (5, 0, -1), (6, 0, -1), (10, 100, -1),
+                         (10, 0, -1), (7, 192, -4), (3, 65, -4), (4, 1 << 31, -4)]:
+        a = list(good); a[idx] = val
+        assert f(*a) == rc, (idx, val)
+    assert k.FUSED_MAX_TOKENS == 64
+    a = list(good); a[3] = 0; a[0] = None
+    assert f(*a) == 0 and k.dsv4_last_launch_count() == 0
+    for idx in (0, 1, 2, 11, 12, 13):
+        a = list(good); a[idx] = None
+        assert f(*a) == -2, idx
+    for idx in (0, 1, 2, 11, 13):
+        a = list(good); a[idx] = P + 8
+        assert f(*a) == -3, idx
 
 
 def test_o_proj_workspace_bytes(lib):

@@ -303,3 +303,54 @@ def test_o_proj_random_shapes(dev, i):
                                 heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank,
                                 hidden=w.hidden)
     assert_chain_matches(og, out64, what=str(w))
+
+
+# ---------------------------------------------------------------------------
+# quantiser fused into wo_a (decode sizes)
+# ---------------------------------------------------------------------------
+
+def _fused_and_separate(w, d, dev):
+    import deepseek_v4_attention_gb300 as k
+    o, pos, cache = d["o"].to(dev), d["positions"].to(dev), d["cache"].to(dev)
+    wa, was = d["wo_a"].to(dev), d["wo_a_scale"].to(dev)
+    zf = k.dsv4_inv_rope_grouped_wo_a(o, pos, cache, wa, was, w.n_groups, w.heads_per_group,
+                                      w.o_lora_rank)
+    assert k.dsv4_last_launch_count() == 1
+    sf = k.dsv4_device_status(clear=True)
+    q, sc = k.dsv4_inv_rope_fp8_quant(o, pos, cache, w.n_groups, w.heads_per_group)
+    zs = k.dsv4_grouped_wo_a(q, sc, wa, was, w.n_groups, w.o_lora_rank)
+    ss = k.dsv4_device_status(clear=True)
+    return to_bits(zf), to_bits(zs), sf, ss
+
+
+# (T, G, hpg, R): split-K cluster tiles (even hpg, few tiles), one CTA per tile
+# (hpg = 1, or 128 tiles), ragged T, a single token
+@pytest.mark.parametrize("T,G,hpg,R", [(1, 2, 2, 128), (7, 8, 8, 1024), (16, 2, 2, 128),
+                                       (33, 4, 4, 256), (64, 8, 8, 1024), (64, 16, 8, 1024),
+                                       (5, 3, 1, 384)])
+def test_fused_wo_a_equals_quant_then_gemm(dev, T, G, hpg, R):
+    """The fused producer runs the quantiser's arithmetic: z is bit-identical to
+    dsv4_grouped_wo_a of dsv4_inv_rope_fp8_quant's output, and within the GEMM
+    tolerance of the oracle."""
+    w = di.Workload("fused", T=T, n_groups=G, heads_per_group=hpg, o_lora_rank=R, hidden=256,
+                    max_pos=4096, seed=T * 31 + G)
+    d = di.make_inputs(w, with_wo_b=False)
+    zf, zs, sf, ss = _fused_and_separate(w, d, dev)
+    assert sf == 0 and ss == 0
+    assert np.array_equal(zf, zs), "fused z differs from quant + grouped GEMM"
+    x, xs = oracle.inv_rope_fp8_quant(d["o"], d["positions"], d["cache"], G, hpg)
+    _, z64 = oracle.grouped_gemm(x, xs, d["wo_a"], d["wo_a_scale"], T, G, hpg * 512, R,
+                                 want_fp64=True)
+    assert gemm_rel_err(zf, z64) <= GEMM_RTOL
+
+
+def test_fused_wo_a_out_of_range_position(dev):
+    """A position outside [0, max_pos) is recorded (DSV4_ERR_RANGE) and that
+    token's rope lanes are quantised unrotated, exactly as by the quantiser."""
+    import deepseek_v4_attention_gb300 as k
+    w = di.WORKLOADS["decode"].with_tokens(9, seed=5)
+    d = di.make_inputs(w, with_wo_b=False)
+    d["positions"][3] = w.max_pos + 7
+    zf, zs, sf, ss = _fused_and_separate(w, d, dev)
+    assert k.STATUS[sf] == "DSV4_ERR_RANGE" and ss == sf
+    assert np.array_equal(zf, zs)
