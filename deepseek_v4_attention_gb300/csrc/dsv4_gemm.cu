@@ -33,6 +33,13 @@
 //                    FP8 re-quantisation (one thread holds one whole 128-block);
 //                    the results leave through a swizzled shared-memory box
 //                    and a TMA store (coalesced, rows beyond T clipped).
+//   fused A (kFused, decode sizes): the TMA thread loads, instead of the FP8 A
+//                    tile, the k-block's bf16 slice of the attention output
+//                    into a small ring; four producer warps after the
+//                    epilogue warps apply the quantiser's arithmetic to it
+//                    and write the FP8 A tile and its scale bytes into the
+//                    stage (the stage's full barrier then counts six
+//                    arrivals).
 // The producer and the MMA issuer are single-thread loops: their per-k-block
 // instruction chain is what feeds the tensor pipe.
 //
