@@ -191,7 +191,16 @@ void launch_bf16_u(const void* o, const int64_t* positions, const float* cache, 
   const int threads = 256;
   const int64_t items = T * (H / kU);
   int64_t blocks = (items * 32 + threads - 1) / threads;
-  const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * (2048 / threads);
+  // one wave: as many blocks as are resident at once (the registers bound it;
+  // a second, partial wave of blocks measured 2-3 % slower)
+  static int resident[64] = {0};
+  int& per_sm = resident[dev.device >= 0 && dev.device < 64 ? dev.device : 0];
+  if (per_sm == 0 &&
+      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, inv_rope_bf16_kernel<kU>, threads,
+                                                     0) != cudaSuccess ||
+       per_sm <= 0))
+    per_sm = 2048 / threads;
+  const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * per_sm;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
   inv_rope_bf16_kernel<kU><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
@@ -207,7 +216,16 @@ void launch_u(const void* o, const int64_t* positions, const float* cache, int64
   const int threads = 256;
   const int64_t items = T * (H / kU);
   int64_t blocks = (items * 32 + threads - 1) / threads;
-  const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * (2048 / threads);
+  // one wave: as many blocks as are resident at once (the registers bound it;
+  // a second, partial wave of blocks measured 2-3 % slower)
+  static int resident[64] = {0};
+  int& per_sm = resident[dev.device >= 0 && dev.device < 64 ? dev.device : 0];
+  if (per_sm == 0 &&
+      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, inv_rope_fp8_quant_kernel<kU>, threads,
+                                                     0) != cudaSuccess ||
+       per_sm <= 0))
+    per_sm = 2048 / threads;
+  const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * per_sm;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
   inv_rope_fp8_quant_kernel<kU><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
