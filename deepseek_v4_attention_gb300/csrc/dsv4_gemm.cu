@@ -61,6 +61,7 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBK = 128;
 constexpr int kTmemCols = 512;
+constexpr int kRasterM = 16;   // m-blocks per raster group (G = 1); 8 measured worse
 
 constexpr uint32_t kSfaBytes = kBM * 4;    // 512 B
 
@@ -133,10 +134,28 @@ struct Params {
   const float* cache;      // fp32 [max_pos][64]
   int64_t max_pos;
   int H, hpg;
+  int raster_m;            // > 0: tiles in groups of raster_m m-blocks (G = 1), see tile_coords
 };
 
+// Tile order.  Default: m-blocks fastest, then column tiles, then groups (the
+// column tiles of one group's m-block run in the same wave and share its A tile
+// in L2).  raster_m > 0 (a single group with many m-blocks, the dense wo_b):
+// groups of raster_m m-blocks, column tiles within a group, so that a wave
+// re-reads only its group's share of A (measured at T = 4096: DRAM reads of
+// wo_b 536 -> 411 MB).
 __device__ __forceinline__ void tile_coords(const Params& p, int tile, int& g, int& n_blk,
                                             int& m_blk) {
+  if (p.raster_m > 0) {
+    const int per_group = p.raster_m * p.n_tiles;
+    const int grp = tile / per_group;
+    const int idx = tile - grp * per_group;
+    const int rest_m = p.m_tiles - grp * p.raster_m;
+    const int m_in = rest_m < p.raster_m ? rest_m : p.raster_m;   // the last group may be short
+    n_blk = idx / m_in;
+    m_blk = grp * p.raster_m + (idx - n_blk * m_in);
+    g = 0;
+    return;
+  }
   m_blk = tile % p.m_tiles;
   const int rest = tile / p.m_tiles;
   n_blk = rest % p.n_tiles;
@@ -871,6 +890,7 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   p.max_pos = q.max_pos;
   p.H = q.heads;
   p.hpg = q.heads_per_group;
+  p.raster_m = (q.G == 1 && p.m_tiles > kRasterM) ? kRasterM : 0;
 
   // persistent: one CTA per SM; split-K: one cluster of kSplit CTAs per tile
   const int grid = kSplit == 1 ? (p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms)
