@@ -11,10 +11,11 @@
 // or 256, see Cfg):
 //   warp 0, lane 0   TMA producer: A tile (128 tokens x 128 k) and B tile
 //                    (kBN rows x 128 k), both with the 128-byte swizzle.
-//   warp 1, lane 0   MMA issuer: per k-block, tcgen05.cp of the stage's scale
-//                    factors into the stage's TMEM columns, then four
-//                    tcgen05.mma (K = 32) from precomputed descriptors, then
-//                    one commit that frees the stage.
+//   warp 1, lane 0   MMA issuer: at the first k-block of each pack of four,
+//                    tcgen05.cp of the stage's scale factors into a TMEM
+//                    region; per k-block four tcgen05.mma (K = 32) from
+//                    precomputed descriptors, then one commit that frees the
+//                    stage.
 //   warp 2           scale-factor warp: each stage has its own scale-factor
 //                    slot, filled for the stage's k-block and completed on the
 //                    stage's full barrier (which therefore counts two
@@ -25,8 +26,7 @@
 //                    (TMEM column c of lane r = row 32 c + r); it expands the
 //                    raw 128 x 128 UE8M0 weight bytes into the kBN-row B
 //                    scales.  The stage's empty barrier (committed after the
-//                    MMAs that read the stage) guards both the slot and its
-//                    TMEM columns.
+//                    MMAs that read the stage) guards the slot.
 //   warps 3..        epilogue: per warp a 32-row x 128-column slice of the fp32
 //                    accumulator to registers (tcgen05.ld), release of the
 //                    accumulator, then bf16 conversion or the fused per-128
@@ -356,6 +356,13 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      // A pack's scale words serve its four k-blocks (the scale-factor id picks
+      // the byte), so they are copied to TMEM once per pack, into region
+      // (packs so far) mod kStages.  A region is rewritten kStages packs later,
+      // by which time the full-barrier wait of that stage proves every MMA at
+      // least kStages k-blocks back complete, the old pack's included.  (The
+      // fused A role writes one byte per stage; it copies every stage.)
+      int sf_region = kStages - 1;
       for (int tile = first_tile<kSplit>(); tile < p.num_tiles && ok;
            tile += tile_stride<kSplit>(p)) {
         if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
@@ -365,9 +372,11 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           // the stage's scale factors arrived with its operands (same barrier)
-          const uint32_t sf_col =
-              tmem_base + static_cast<uint32_t>(C::kSfCol0 + stage * C::kSfColsPerSlot);
-          if (!kBf16) {
+          const bool pack_start = kb == kb_begin<kSplit>(p) || (kb & 3) == 0;
+          if (pack_start) sf_region = (sf_region + 1 == kStages) ? 0 : sf_region + 1;
+          const uint32_t sf_col = tmem_base + static_cast<uint32_t>(
+              C::kSfCol0 + (kFused ? stage : sf_region) * C::kSfColsPerSlot);
+          if (!kBf16 && (kFused || pack_start)) {
             const uint64_t sd = sfdesc0 + ((stage * C::kSfSlotBytes) >> 4);
             tmem_cp_32x128b_x4(sf_col, sd);                     // A: the slot's first 512 B
 #pragma unroll
