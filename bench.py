@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--summarize-traffic", metavar="CSV", default=None,
+                    help="print the per-launch DRAM lines of profiles/dram_traffic_full_T4096.txt "
+                         "from an ncu --csv launch list (no GPU needed) and exit")
     ap.add_argument("--workload", default="full",
                     choices=["full", "tiny", "decode", "prefill", "quant1k", "quant8k", "quant32k",
                              "decode_bf16", "prefill_bf16"],
@@ -175,6 +178,49 @@ def recorded_traffic(kernel: str) -> float | None:
             elif tok[0] == kernel:
                 vals.append(float(tok[1]) + float(tok[2]))
     return sum(vals) / len(vals) if vals else None
+
+
+TRAFFIC_SOURCES = ("dsv4_gemm.cu", "dsv4_quant.cu", "dsv4_device.cuh")
+
+
+def summarize_traffic(csv_path: str) -> str:
+    """The body of profiles/dram_traffic_full_T4096.txt from an ncu launch list
+    (--csv with gpu__time_duration.sum, dram__bytes_read.sum and
+    dram__bytes_write.sum): the sha256 of the kernel sources, then one line per
+    launch, grouped by kernel.  recorded_traffic() reads it back."""
+    import csv
+    import hashlib
+    launches: dict[str, tuple[str, dict]] = {}
+    header = None
+    with open(csv_path, newline="") as f:
+        for row in csv.reader(f):
+            if "Kernel Name" in row:
+                header = row
+                continue
+            if header is None or len(row) != len(header):
+                continue
+            rec = dict(zip(header, row))
+            name, metrics = launches.setdefault(rec["ID"], (rec["Kernel Name"], {}))
+            metrics[rec["Metric Name"]] = float(rec["Metric Value"].replace(",", ""))
+
+    def kernel_of(name: str) -> str:
+        if "inv_rope" in name:
+            return "quant"
+        return "wo_a" if "<256, 1," in name else "wo_b"   # the re-quantising epilogue
+
+    csrc = os.path.join(ROOT, "deepseek_v4_attention_gb300", "csrc")
+    lines = []
+    for src in TRAFFIC_SOURCES:
+        with open(os.path.join(csrc, src), "rb") as g:
+            lines.append(f"source {src} {hashlib.sha256(g.read()).hexdigest()}")
+    lines.append("# kernel  read_bytes  write_bytes  duration_us (ten launches each)")
+    for k in ("quant", "wo_a", "wo_b"):
+        for name, m in launches.values():
+            if kernel_of(name) == k:
+                lines.append(f"{k} {m['dram__bytes_read.sum'] / 1e6:.1f}e6 "
+                             f"{m['dram__bytes_write.sum'] / 1e6:.1f}e6 "
+                             f"{m['gpu__time_duration.sum'] / 1e3:.1f}")
+    return "\n".join(lines)
 
 
 def measured_peaks() -> tuple[dict, str]:
@@ -643,6 +689,9 @@ def run_workload(args, ws, rank, local):
 
 def main():
     args = parse()
+    if args.summarize_traffic:
+        print(summarize_traffic(args.summarize_traffic))
+        return
     ws, rank, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, ws, rank)
