@@ -377,11 +377,13 @@ def _dequant_torch(codes_u8, exps):
     return codes_u8.view(torch.float8_e4m3fn).to(torch.float64) * torch.exp2(exps.to(torch.float64))
 
 
-def test_grouped_gemm_matches_einsum_in_float64(oracle_mod):
+@pytest.mark.parametrize("D", [512, 1152])
+def test_grouped_gemm_matches_einsum_in_float64(oracle_mod, D):
     """The pages restate the grouped product as einsum 'tgd,grd->tgr' (sglang
     bf16 fallback) and as bmm over wo_a viewed [G, R, D] (vLLM): compare with
-    torch.einsum in float64 on the dequantised operands (torch's own FP8 decode)."""
-    T, G, D, R = 9, 3, 512, 256
+    torch.einsum in float64 on the dequantised operands (torch's own FP8 decode).
+    D = 1152: nine scale blocks in three packed words, the last one partial."""
+    T, G, R = 9, 3, 256
     Tal = oracle_mod.tma_aligned_tokens(T)
     x, xs = di.random_fp8_activation(T, G, D, seed=11, tma_aligned_T=Tal)
     w, ws = di.fp8_block_weight(G * R, D, seed=12)
