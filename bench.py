@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--tokens", type=int, default=None, help="tokens per GPU (default 4096)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other synthetic workloads (decode, prefill, quant sweep) that "
+                         "the default run times after the full O-projection")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--summarize-traffic", metavar="CSV", default=None,
@@ -109,22 +112,34 @@ def config_of(w: di.Workload, n_gpus: int) -> dict:
 
 # ---------------------------------------------------------------- clocks --
 class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every INTERVAL_MS while the
+    `with` block runs.  The block starts only once the sampler has produced its
+    first sample (taken before the timed region, and not counted)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.lines = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        self.pre_taken = False
+        if self.proc is not None:
+            import select
+            ready, _, _ = select.select([self.proc.stdout], [], [], 3.0)
+            if ready:
+                self.proc.stdout.readline()          # the sample before the region
+                self.pre_taken = True
         return self
 
     def __exit__(self, *exc):
@@ -137,24 +152,29 @@ class ClockSampler:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            if not self.pre_taken:
+                self.lines = self.lines[1:]          # the sample before the region
 
     def summary(self) -> dict:
-        sm, mx, reasons = [], None, set()
+        sm, mx, power, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
+        for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
             try:
                 sm.append(float(f[1]))
                 mx = float(f[2])
+                power.append(float(f[3]))
             except ValueError:
                 continue
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None,
+                "interval_ms": self.INTERVAL_MS}
 
 
 def recorded_traffic(kernel: str) -> float | None:
@@ -229,6 +249,86 @@ def measured_peaks() -> tuple[dict, str]:
         with open(p) as f:
             return json.load(f), "measured"
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# Dense tensor-core work per SM and clock of the MMAs the kernels issue
+# (tcgen05.mma, one CTA per SM): kind::mxf8f6f4 with e4m3 operands, 128 x 256
+# x 32 multiply-adds in 128 cycles = 16384 flop per clock; kind::f16 with bf16
+# operands half of that.  152 SMs at 1.81 GHz give the nominal 4.5 PFLOP/s FP8.
+MMA_FLOP_PER_CLK_SM = {"e4m3": 16384.0, "bf16": 8192.0}
+SUSTAINED_REGION_S = 1.0   # timed regions at least this long use the sustained peak
+
+
+def tensor_peak(peaks: dict, src: str, timed_s: float, dtype: str) -> tuple[float, str]:
+    """The measured tensor peak for a contraction of `dtype` timed inside a
+    region of timed_s seconds: the burst cuBLAS bf16 figure for a short region,
+    the sustained one for a region of a second or more; FP8 = 2 x bf16 (the
+    nominal dense ratio)."""
+    ratio = 2.0 if dtype == "e4m3" else 1.0
+    if timed_s >= SUSTAINED_REGION_S and "bf16_tflops_sustained" in peaks:
+        base, which = peaks["bf16_tflops_sustained"], "bf16_tflops_sustained"
+    else:
+        base, which = peaks["bf16_tflops"], "bf16_tflops (burst)"
+    rule = f"{src}: {which}" + (" x 2 (fp8 = 2 x bf16)" if ratio == 2.0 else "") + \
+        f", timed region {timed_s * 1e3:.1f} ms"
+    return ratio * base, rule
+
+
+def add_roofline(stage: dict, peaks: dict, src: str, timed_s: float, clocks: dict,
+                 num_sms: int, dtype: str = "e4m3") -> dict:
+    """Fills peak / frac of one stage; for a tensor-bound stage also the
+    clock-matched MMA peak (per-SM rate x SMs x the median sampled SM clock)
+    and the achieved TFLOP/s per GHz of that clock."""
+    if stage["bound"] == "hbm":
+        stage["peak"], stage["peak_rule"] = peaks["hbm_gbs"], f"{src}: hbm_gbs"
+    else:
+        stage["peak"], stage["peak_rule"] = tensor_peak(peaks, src, timed_s, dtype)
+        mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz")
+        if mhz:
+            cm = MMA_FLOP_PER_CLK_SM[dtype] * num_sms * mhz * 1e6 / 1e12
+            stage["clock_matched"] = {"peak": cm, "frac": stage["achieved"] / cm,
+                                      "sm_mhz": mhz, "unit": "TFLOP/s"}
+            stage["tflops_per_ghz"] = stage["achieved"] / (mhz / 1e3)
+    stage["frac"] = stage["achieved"] / stage["peak"]
+    return stage
+
+
+def gpu_local_cpus(local_rank: int) -> set[int] | None:
+    """CPUs on the NUMA node the GPU is attached to (sysfs of its PCI device),
+    or None when that cannot be read."""
+    try:
+        bus = subprocess.run(["nvidia-smi", "-i", str(local_rank), "--query-gpu=pci.bus_id",
+                              "--format=csv,noheader"], capture_output=True, text=True,
+                             timeout=20).stdout.strip()
+        with open(f"/sys/bus/pci/devices/{bus[-12:].lower()}/local_cpulist") as f:
+            text = f.read().strip()
+    except (OSError, subprocess.SubprocessError):
+        return None
+    cpus = set()
+    for part in text.split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    cpus &= os.sched_getaffinity(0)
+    return cpus or None
+
+
+def copy_gbs(dst: torch.Tensor, src: torch.Tensor, dev, reps: int = 5) -> float:
+    """GB/s of one cudaMemcpyAsync of src into dst (pinned host <-> device),
+    timed with CUDA events on the copying stream after one untimed copy."""
+    s = torch.cuda.Stream(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        dst.copy_(src, non_blocking=True)
+        e0.record(s)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        e1.record(s)
+    torch.cuda.synchronize(dev)
+    return src.numel() * src.element_size() * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
 
 
 # ------------------------------------------------------------- our arm --
@@ -307,10 +407,20 @@ def run_ours(args, ws, rank, local):
     e2e = None
     if not args.no_e2e:
         nbuf = 2
-        o_h = [host["o"].pin_memory() for _ in range(nbuf)]
-        p_h = [host["positions"].pin_memory() for _ in range(nbuf)]
-        out_h = [torch.empty(w.T, w.hidden, dtype=torch.bfloat16).pin_memory()
-                 for _ in range(nbuf)]
+        # Pinned host buffers on the NUMA node the GPU is attached to (pages
+        # are placed where the allocating thread runs), as a serving process
+        # bound to its GPU's CPUs would hold them.
+        saved_affinity = os.sched_getaffinity(0)
+        local_cpus = gpu_local_cpus(local)
+        if local_cpus:
+            os.sched_setaffinity(0, local_cpus)
+        try:
+            o_h = [host["o"].pin_memory() for _ in range(nbuf)]
+            p_h = [host["positions"].pin_memory() for _ in range(nbuf)]
+            out_h = [torch.empty(w.T, w.hidden, dtype=torch.bfloat16).pin_memory()
+                     for _ in range(nbuf)]
+        finally:
+            os.sched_setaffinity(0, saved_affinity)
         o_d = [torch.empty_like(d["o"]) for _ in range(nbuf)]
         p_d = [torch.empty_like(d["positions"]) for _ in range(nbuf)]
         out_d = [torch.empty_like(out) for _ in range(nbuf)]
@@ -356,50 +466,72 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize(dev)
         barrier()
         e_ms = max_over_ranks(a0.elapsed_time(a1))
-        e2e = {"value": job_throughput(w.T, ws, e2e_steps, e_ms), "unit": UNIT,
-               "h2d_bytes_per_step": o_h[0].numel() * 2 + p_h[0].numel() * 8,
-               "d2h_bytes_per_step": out_h[0].numel() * 2, "steps": e2e_steps,
+        h2d_bytes = o_h[0].numel() * 2 + p_h[0].numel() * 8
+        d2h_bytes = out_h[0].numel() * 2
+        # the host link measured on this machine in this run: one copy of the
+        # step's o in, one of its out back, from/to the same pinned buffers
+        h2d_gbs = copy_gbs(o_d[0], o_h[0], dev)
+        d2h_gbs = copy_gbs(out_h[0], out_d[0], dev)
+        bound_ms = max(h2d_bytes / (h2d_gbs * 1e9) * 1e3, d2h_bytes / (d2h_gbs * 1e9) * 1e3,
+                       ms_step)
+        value_e2e = job_throughput(w.T, ws, e2e_steps, e_ms)
+        bound = job_throughput(w.T, ws, 1, bound_ms)
+        e2e = {"value": value_e2e, "unit": UNIT,
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+               "steps": e2e_steps,
                "pipeline": "input copy / compute / read-back of consecutive steps overlap "
-                           "(two buffers, three streams)"}
+                           "(two buffers, three streams)",
+               "link": {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
+                        "pinned_on_gpu_numa_node": bool(local_cpus),
+                        "bound": bound, "frac_of_bound": value_e2e / bound,
+                        "bound_rule": "T / max(h2d bytes / h2d GB/s, d2h bytes / d2h GB/s, "
+                                      "device step time)"}}
+        del o_h, p_h, out_h, o_d, p_d, out_d
 
     # --- roofline of the dominant kernel (the largest stage time)
     peaks, src = measured_peaks()
+    clocks = clk.summary()
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    timed_s = ms_total / 1e3
     T, G, R, D, Hd = w.T, w.n_groups, w.o_lora_rank, w.D, w.hidden
     fl_a = 2.0 * T * G * R * D
     fl_b = 2.0 * T * Hd * G * R
     quant_bytes = T * w.H * (1024 + 512 + 4) + T * (8 + 256)
-    fp8_peak = 2.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])  # fp8 = 2 x bf16
     stages = {
         "quant": {"ms": stage_ms[0], "bound": "hbm", "algorithmic": quant_bytes,
-                  "achieved": quant_bytes / (stage_ms[0] * 1e-3) / 1e9, "unit": "GB/s",
-                  "peak": peaks["hbm_gbs"]},
+                  "achieved": quant_bytes / (stage_ms[0] * 1e-3) / 1e9, "unit": "GB/s"},
         "wo_a": {"ms": stage_ms[1], "bound": "tensor", "algorithmic": fl_a,
-                 "achieved": fl_a / (stage_ms[1] * 1e-3) / 1e12, "unit": "TFLOP/s",
-                 "peak": fp8_peak},
+                 "achieved": fl_a / (stage_ms[1] * 1e-3) / 1e12, "unit": "TFLOP/s"},
         "wo_b": {"ms": stage_ms[2], "bound": "tensor", "algorithmic": fl_b,
-                 "achieved": fl_b / (stage_ms[2] * 1e-3) / 1e12, "unit": "TFLOP/s",
-                 "peak": fp8_peak},
+                 "achieved": fl_b / (stage_ms[2] * 1e-3) / 1e12, "unit": "TFLOP/s"},
     }
-    for s in stages.values():
-        s["frac"] = s["achieved"] / s["peak"]
+    for s_ in stages.values():
+        add_roofline(s_, peaks, src, timed_s, clocks, num_sms)
     dom = max(stages, key=lambda n: stages[n]["ms"])
     ds = stages[dom]
     roofline = {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
                 "peak": ds["peak"], "unit": ds["unit"], "frac": ds["frac"],
                 "traffic": recorded_traffic(dom) if w.T == 4096 else None,
-                "peak_source": f"{src}: " + ("fp8 = 2 x bf16_tflops_sustained"
-                                              if ds["bound"] == "tensor" else "hbm_gbs")}
+                "peak_source": ds["peak_rule"]}
+    if "clock_matched" in ds:
+        roofline["clock_matched"] = ds["clock_matched"]
 
-    clocks = clk.summary()
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-        "data": "synthetic (seeded; random FP8 block-scaled weights)",
+        "data": "synthetic (seeded; FP8 block-scaled weights drawn in stored form)",
         "config": config_of(w, ws), "clocks": clocks, "e2e": e2e,
         "gpu_launches": launches, "roofline": roofline,
         "stages": {n: {kk: v for kk, v in s.items()} for n, s in stages.items()},
     }
+    if rank == 0 and not args.no_configs and ws == 1:
+        result["configs"] = {}
+        for name in CONFIG_WORKLOADS:
+            r = run_workload(name, max(args.steps, 200), max(args.warmup, 3), local)
+            result["configs"][name] = r
+            result["gpu_launches_configs"] = result.get("gpu_launches_configs", 0) + \
+                r["gpu_launches"]
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if ws > 1:
@@ -548,20 +680,28 @@ def _graph_ms(fn, steps: int, stream) -> dict:
             "p50_ms": q(0.5), "p90_ms": q(0.9)}
 
 
-def run_workload(args, ws, rank, local):
+# The other synthetic workloads the default run times after the full
+# O-projection, each by CUDA-graph replay: tiny (correctness-sized), decode
+# (weight-read bound wo_a), prefill (FP8 tensor bound wo_a) and the quantiser
+# sweep.
+CONFIG_WORKLOADS = ("tiny", "decode", "prefill", "quant1k", "quant8k", "quant32k")
+
+
+def run_workload(name: str, steps: int, warmup: int, local: int) -> dict:
     """One of the smaller synthetic workloads: quant (+ grouped wo_a).  Each step
     uses the next of several rotating input sets whose total exceeds 3x L2, so
-    that weights and activations come from HBM, not from the previous step."""
+    that weights and activations come from HBM, not from the previous step.
+    The quantiser sweep's large o tensors are drawn on the device (same recipe,
+    the device's random stream) to keep the host's generation time short."""
     import deepseek_v4_attention_gb300 as k
 
-    if ws > 1:
-        raise SystemExit("--workload other than full runs on one GPU")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    bf16 = args.workload.endswith("_bf16")
-    w = di.WORKLOADS[args.workload.replace("_bf16", "")]
+    bf16 = name.endswith("_bf16")
+    w = di.WORKLOADS[name.replace("_bf16", "")]
     gemm = not w.name.startswith("quant")
-    host = di.make_inputs(w, with_wo_b=False)
+    on_device = w.name in ("quant8k", "quant32k")
+    host = di.make_inputs(w, with_wo_b=False, o_device=dev if on_device else None)
     if bf16:   # the model served without FP8: bf16 wo_a, quantize=False
         host["wo_a"] = di.bf16_weight(w.n_groups * w.o_lora_rank, w.D, w.seed + 303)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -583,6 +723,7 @@ def run_workload(args, ws, rank, local):
             st["z"] = torch.empty(w.T, w.n_groups, w.o_lora_rank, dtype=torch.bfloat16,
                                   device=dev)
         sets.append(st)
+    del host
     stream = torch.cuda.Stream(dev)
 
     def quant(i):
@@ -620,57 +761,64 @@ def run_workload(args, ws, rank, local):
             wo_a(i)
 
     with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 3)):
+        for i in range(max(warmup, 3)):
             step(i)
     torch.cuda.synchronize()
     launches_per_step = 2 if gemm else 1
     with ClockSampler(local) as clk:
-        t_step = _graph_ms(step, args.steps, stream)
-        t_q = _graph_ms(quant, args.steps, stream)
-        t_a = _graph_ms(wo_a, args.steps, stream) if gemm else None
-        t_f = _graph_ms(wo_a_fused, args.steps, stream) if fused else None
+        t_step = _graph_ms(step, steps, stream)
+        t_q = _graph_ms(quant, steps, stream)
+        t_a = _graph_ms(wo_a, steps, stream) if gemm else None
+        t_f = _graph_ms(wo_a_fused, steps, stream) if fused else None
     ms_step, ms_q = t_step["ms"], t_q["ms"]
     ms_a = t_a["ms"] if gemm else 0.0
     spread = lambda t: {k_: round(v, 5) for k_, v in t.items() if k_ != "ms"}
     if k.dsv4_device_status(clear=True) != 0:
         raise RuntimeError("device status error")
     peaks, src = measured_peaks()
+    clocks = clk.summary()
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    dtype = "bf16" if bf16 else "e4m3"
     qbytes = w.T * w.H * (1024 + (1024 if bf16 else 512 + 4)) + w.T * (8 + 256)
     stages = {"quant": {"ms": ms_q, "bound": "hbm", "algorithmic": qbytes,
-                        "achieved": qbytes / (ms_q * 1e-3) / 1e9, "unit": "GB/s",
-                        "peak": peaks["hbm_gbs"], **spread(t_q)}}
+                        "achieved": qbytes / (ms_q * 1e-3) / 1e9, "unit": "GB/s", **spread(t_q)}}
     if gemm:
         fl = 2.0 * w.T * w.n_groups * w.o_lora_rank * w.D
         by = (w.n_groups * w.o_lora_rank * w.D + w.n_groups * w.T * w.D) * esz + \
             w.T * w.n_groups * w.o_lora_rank * 2
-        tensor_peak = (1.0 if bf16 else 2.0) * peaks.get("bf16_tflops_sustained",
-                                                          peaks["bf16_tflops"])
-        if w.name == "decode":      # weight-read bound: bytes against HBM
+        if w.name in ("decode", "tiny"):      # weight-read bound: bytes against HBM
             stages["wo_a"] = {"ms": ms_a, "bound": "hbm", "algorithmic": by,
                               "achieved": by / (ms_a * 1e-3) / 1e9, "unit": "GB/s",
-                              "peak": peaks["hbm_gbs"], **spread(t_a)}
+                              **spread(t_a)}
         else:
             stages["wo_a"] = {"ms": ms_a, "bound": "tensor", "algorithmic": fl,
                               "achieved": fl / (ms_a * 1e-3) / 1e12, "unit": "TFLOP/s",
-                              "peak": tensor_peak, **spread(t_a)}
+                              **spread(t_a)}
     if fused:   # one kernel: o and the weights in, z out (not part of the step)
         fb = w.T * w.H * 1024 + w.T * (8 + 256) + w.n_groups * w.o_lora_rank * w.D + \
             w.T * w.n_groups * w.o_lora_rank * 2
         stages["fused_quant_wo_a"] = {"ms": t_f["ms"], "bound": "hbm", "algorithmic": fb,
                                       "achieved": fb / (t_f["ms"] * 1e-3) / 1e9, "unit": "GB/s",
-                                      "peak": peaks["hbm_gbs"], **spread(t_f)}
-    for s_ in stages.values():
-        s_["frac"] = s_["achieved"] / s_["peak"]
+                                      **spread(t_f)}
+    for n_, s_ in stages.items():
+        region_s = {"quant": t_q, "wo_a": t_a, "fused_quant_wo_a": t_f}[n_]["ms"] * steps / 1e3
+        add_roofline(s_, peaks, src, region_s, clocks, num_sms, dtype)
     dom = max((n for n in stages if n != "fused_quant_wo_a"), key=lambda n: stages[n]["ms"])
     ds = stages[dom]
-    result = {
+    roofline = {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
+                "peak": ds["peak"], "unit": ds["unit"], "frac": ds["frac"],
+                "traffic": None, "peak_source": ds["peak_rule"]}
+    if "clock_matched" in ds:
+        roofline["clock_matched"] = ds["clock_matched"]
+    return {
         "metric": METRIC, "value": w.T / (ms_step * 1e-3), "unit": UNIT, "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if bf16 else "e4m3",
-        "data": "synthetic (seeded; random " + ("bf16" if bf16 else "FP8 block-scaled") +
-                " weights)",
-        "config": {"workload": f"{args.workload}: T={w.T}, {w.H} heads x 512 ({w.n_groups} "
+        "dtype": dtype,
+        "data": "synthetic (seeded; " + ("bf16 weights" if bf16 else
+                                         "FP8 block-scaled weights drawn in stored form") +
+                ("; o drawn on the device" if on_device else "") + ")",
+        "config": {"workload": f"{name}: T={w.T}, {w.H} heads x 512 ({w.n_groups} "
                                f"groups x {w.heads_per_group})" +
                                (f", o_lora_rank {w.o_lora_rank}, " + ("bf16 inverse RoPE + bf16 "
                                 "grouped wo_a" if bf16 else "quant + grouped wo_a")
@@ -678,13 +826,9 @@ def run_workload(args, ws, rank, local):
                    "timing": "CUDA-graph replay, graphs of 10 calls; p10/p50/p90 over the "
                              "replays", "input_sets": nsets,
                    "l2": f"{nsets} rotating input sets of {set_bytes / 1e6:.1f} MB (>= 3x L2)"},
-        "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
-                     "peak": ds["peak"], "unit": ds["unit"], "frac": ds["frac"],
-                     "traffic": None, "peak_source": src},
-        "stages": stages, "step_spread": spread(t_step),
+        "clocks": clocks, "gpu_launches": launches_per_step * steps,
+        "roofline": roofline, "stages": stages, "step_spread": spread(t_step),
     }
-    return result
 
 
 def main():
@@ -696,7 +840,9 @@ def main():
     if args.impl == "reference":
         res = run_reference(args, ws, rank)
     elif args.workload != "full":
-        res = run_workload(args, ws, rank, local)
+        if ws > 1:
+            raise SystemExit("--workload other than full runs on one GPU")
+        res = run_workload(args.workload, args.steps, args.warmup, local)
     else:
         res = run_ours(args, ws, rank, local)
     if rank == 0 and res is not None:

@@ -67,6 +67,20 @@ def load_library() -> ctypes.CDLL:
     lib.dsv4_o_proj_with_events.restype = I
     lib.dsv4_o_proj_static.argtypes = [P, P, P, I64, I64, I, I, I, I, I, I, I, P, P, P, P, P, P]
     lib.dsv4_o_proj_static.restype = I
+    lib.dsv4_o_proj_partial.argtypes = [P, P, P, I64, I64, I, I, I, I, I, I, I, P, P, P, P, P, P,
+                                        ctypes.c_size_t, P]
+    lib.dsv4_o_proj_partial.restype = I
+    lib.dsv4_sum_partials.argtypes = [P, I, I64, P, P]
+    lib.dsv4_sum_partials.restype = I
+    lib.dsv4_rope_quant_unsupported_reason.argtypes = [I, I, I, ctypes.POINTER(ctypes.c_char_p)]
+    lib.dsv4_rope_quant_unsupported_reason.restype = I
+    lib.dsv4_o_proj_prequant_workspace_bytes.argtypes = [I64, I, I]
+    lib.dsv4_o_proj_prequant_workspace_bytes.restype = ctypes.c_size_t
+    lib.dsv4_o_proj_prequant.argtypes = [P, P, I64, I, I, I, I, I, P, P, P, P, P, P,
+                                         ctypes.c_size_t, P]
+    lib.dsv4_o_proj_prequant.restype = I
+    lib.dsv4_static_scratch_bytes.argtypes = []
+    lib.dsv4_static_scratch_bytes.restype = ctypes.c_size_t
     lib.dsv4_status_string.argtypes = [I]
     lib.dsv4_status_string.restype = ctypes.c_char_p
     lib.dsv4_device_status.argtypes = [P, I]
@@ -280,6 +294,74 @@ def dsv4_o_proj_workspace_bytes(num_tokens: int, n_groups: int, heads_per_group:
                                                           head_dim, o_lora_rank))
 
 
+def _round256(x: int) -> int:
+    return (x + 255) // 256 * 256
+
+
+def o_proj_workspace_views(workspace: torch.Tensor, num_tokens: int, n_groups: int,
+                           heads_per_group: int, head_dim: int, o_lora_rank: int) -> dict:
+    """Views of the parts of dsv4_o_proj's workspace, in the order and at the
+    256-byte-aligned offsets include/dsv4.h fixes, holding the intermediate
+    results of the last call that used it:
+
+        x   uint8 [G, T, D]        the quantised groups (e4m3 codes)
+        xs  int32 [G, PK, T_al]    their packed UE8M0 scales
+        zq  uint8 [T, G*R]         the per-128 re-quantised bf16 z (e4m3 codes)
+        zs  int32 [PKC, T_al]      their packed UE8M0 scales, PKC = ceil(G*R/512)
+    """
+    T, G, R = num_tokens, n_groups, o_lora_rank
+    D = heads_per_group * head_dim
+    PK = (D // 128 + 3) // 4
+    C = G * R
+    PKC = (C // 128 + 3) // 4
+    T_al = tma_aligned_tokens(T)
+    ws = workspace.view(torch.uint8)
+    off = 0
+
+    def take(nbytes):
+        nonlocal off
+        part = ws[off:off + nbytes]
+        off += _round256(nbytes)
+        return part
+
+    x = take(G * T * D).view(G, T, D)
+    xs = take(G * PK * T_al * 4).view(torch.int32).view(G, PK, T_al)
+    zq = take(T * C).view(T, C)
+    zs = take(PKC * T_al * 4).view(torch.int32).view(PKC, T_al)
+    return {"x": x, "xs": xs, "zq": zq, "zs": zs}
+
+
+def _check_o_proj_weights(wo_a, wo_a_scale, wo_b, wo_b_scale, C: int, D: int) -> int:
+    """dtype, layout and shape checks of the two projections' weights; returns hidden."""
+    for t, n in ((wo_a, "wo_a"), (wo_b, "wo_b")):
+        _cuda(t, n, _FP8)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for t, n in ((wo_a_scale, "wo_a_scale"), (wo_b_scale, "wo_b_scale")):
+        _cuda(t, n, _SCALE8)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    hidden = wo_b.shape[0]
+    if tuple(wo_a.shape) != (C, D) or tuple(wo_b.shape) != (hidden, C):
+        raise ValueError("weight shapes must be wo_a [G*R, D] and wo_b [hidden, G*R]")
+    if tuple(wo_a_scale.shape) != (C // 128, D // 128) or \
+            tuple(wo_b_scale.shape) != (hidden // 128, C // 128):
+        raise ValueError("weight scales must be [rows/128, cols/128]")
+    return hidden
+
+
+def _check_o(o, positions, cos_sin_cache, n_groups, heads_per_group, what):
+    _cuda(o, "o", torch.bfloat16)
+    _cuda(positions, "positions", torch.int64)
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    if o.dim() != 3 or not o.is_contiguous():
+        raise ValueError("o must be a contiguous [T, H, head_dim] tensor")
+    T, H, hd = o.shape
+    if H != n_groups * heads_per_group or positions.numel() != T:
+        raise DSV4Error(-1, f"{what} (head count / positions)")
+    return T, hd
+
+
 def dsv4_o_proj(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
                 wo_a: torch.Tensor, wo_a_scale: torch.Tensor, wo_b: torch.Tensor,
                 wo_b_scale: torch.Tensor, *, n_groups: int, heads_per_group: int,
@@ -292,30 +374,10 @@ def dsv4_o_proj(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.T
     stage_events: optional list of 4 torch.cuda.Event(enable_timing=True),
     recorded before the first kernel and after each of the three kernels."""
     lib = load_library()
-    _cuda(o, "o", torch.bfloat16)
-    _cuda(positions, "positions", torch.int64)
-    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
-    for t, n in ((wo_a, "wo_a"), (wo_b, "wo_b")):
-        _cuda(t, n, _FP8)
-        if not t.is_contiguous():
-            raise ValueError(f"{n} must be contiguous")
-    for t, n in ((wo_a_scale, "wo_a_scale"), (wo_b_scale, "wo_b_scale")):
-        _cuda(t, n, _SCALE8)
-        if not t.is_contiguous():
-            raise ValueError(f"{n} must be contiguous")
-    if o.dim() != 3 or not o.is_contiguous():
-        raise ValueError("o must be a contiguous [T, H, head_dim] tensor")
-    T, H, hd = o.shape
-    if H != n_groups * heads_per_group or positions.numel() != T:
-        raise DSV4Error(-1, "dsv4_o_proj (head count / positions)")
-    hidden = wo_b.shape[0]
+    T, hd = _check_o(o, positions, cos_sin_cache, n_groups, heads_per_group, "dsv4_o_proj")
     C = n_groups * o_lora_rank
     D = heads_per_group * hd
-    if tuple(wo_a.shape) != (C, D) or tuple(wo_b.shape) != (hidden, C):
-        raise ValueError("weight shapes must be wo_a [G*R, D] and wo_b [hidden, G*R]")
-    if tuple(wo_a_scale.shape) != (C // 128, D // 128) or \
-            tuple(wo_b_scale.shape) != (hidden // 128, C // 128):
-        raise ValueError("weight scales must be [rows/128, cols/128]")
+    hidden = _check_o_proj_weights(wo_a, wo_a_scale, wo_b, wo_b_scale, C, D)
     need = dsv4_o_proj_workspace_bytes(T, n_groups, heads_per_group, hd, o_lora_rank)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=o.device)
@@ -339,7 +401,130 @@ def dsv4_o_proj(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.T
     return out
 
 
-STATIC_SCRATCH_BYTES = 64 << 20   # DSV4_STATIC_SCRATCH_BYTES in include/dsv4.h
+def dsv4_o_proj_partial(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                        wo_a: torch.Tensor, wo_a_scale: torch.Tensor, wo_b: torch.Tensor,
+                        wo_b_scale: torch.Tensor, *, n_groups: int, heads_per_group: int,
+                        o_lora_rank: int, nope_dim: int = 448, rope_dim: int = 64,
+                        quant_group_size: int = 128, out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One group range's share of the O-projection (its heads of o, its wo_a
+    rows, its wo_b columns): returns the fp32 partial output [T, hidden]."""
+    lib = load_library()
+    T, hd = _check_o(o, positions, cos_sin_cache, n_groups, heads_per_group,
+                     "dsv4_o_proj_partial")
+    C = n_groups * o_lora_rank
+    hidden = _check_o_proj_weights(wo_a, wo_a_scale, wo_b, wo_b_scale, C, heads_per_group * hd)
+    need = dsv4_o_proj_workspace_bytes(T, n_groups, heads_per_group, hd, o_lora_rank)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=o.device)
+    if out is None:
+        out = torch.empty((T, hidden), dtype=torch.float32, device=o.device)
+    _cuda(out, "out", torch.float32)
+    rc = lib.dsv4_o_proj_partial(o.data_ptr(), positions.data_ptr(), cos_sin_cache.data_ptr(),
+                                 cos_sin_cache.shape[0], T, n_groups, heads_per_group, nope_dim,
+                                 rope_dim, quant_group_size, o_lora_rank, hidden,
+                                 wo_a.data_ptr(), wo_a_scale.data_ptr(), wo_b.data_ptr(),
+                                 wo_b_scale.data_ptr(), out.data_ptr(), workspace.data_ptr(),
+                                 workspace.numel(), _stream(stream))
+    _check(rc, "dsv4_o_proj_partial")
+    return out
+
+
+MAX_PARTIALS = 16   # DSV4_MAX_PARTIALS
+
+
+def dsv4_sum_partials(partials, *, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """bf16(sum of the fp32 partial outputs, in list order) with their shape."""
+    lib = load_library()
+    parts = list(partials)
+    if not parts:
+        raise ValueError("no partials")
+    for t in parts:
+        _cuda(t, "partial", torch.float32)
+        if not t.is_contiguous() or t.shape != parts[0].shape:
+            raise ValueError("partials must be contiguous and of one shape")
+    if out is None:
+        out = torch.empty(parts[0].shape, dtype=torch.bfloat16, device=parts[0].device)
+    _cuda(out, "out", torch.bfloat16)
+    ptrs = (ctypes.c_void_p * len(parts))(*[t.data_ptr() for t in parts])
+    rc = lib.dsv4_sum_partials(ptrs, len(parts), parts[0].numel(), out.data_ptr(),
+                               _stream(stream))
+    _check(rc, "dsv4_sum_partials")
+    return out
+
+
+ROPE_QUANT_NUM_HEADS = 128         # DSV4_ROPE_QUANT_NUM_HEADS
+ROPE_QUANT_HEADS_PER_GROUP = 8     # DSV4_ROPE_QUANT_HEADS_PER_GROUP
+
+
+def rope_quant_unsupported_reason(n_local_heads: int, kv_cache_fp8: bool,
+                                  wo_a_fp8: bool) -> str | None:
+    """None if a layer may take a pre-quantised attention output, else why not."""
+    why = ctypes.c_char_p()
+    rc = load_library().dsv4_rope_quant_unsupported_reason(
+        int(n_local_heads), 1 if kv_cache_fp8 else 0, 1 if wo_a_fp8 else 0, ctypes.byref(why))
+    if rc == DSV4_OK:
+        return None
+    return why.value.decode()
+
+
+def dsv4_o_proj_prequant_workspace_bytes(num_tokens: int, n_groups: int, o_lora_rank: int) -> int:
+    return int(load_library().dsv4_o_proj_prequant_workspace_bytes(num_tokens, n_groups,
+                                                                   o_lora_rank))
+
+
+def dsv4_o_proj_prequant(x_fp8: torch.Tensor, x_scale: torch.Tensor, wo_a: torch.Tensor,
+                         wo_a_scale: torch.Tensor, wo_b: torch.Tensor, wo_b_scale: torch.Tensor,
+                         *, n_groups: int, o_lora_rank: int, out: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The O-projection from a pre-quantised attention output: x_fp8 the
+    [T, n_slots, D] view of a physical [n_slots, T, D] buffer, x_scale the
+    [T, n_slots, PK] view of a physical [n_slots, PK, T_al] one (the RopeQuant
+    layout of rope_quant_attn_out); the first n_groups slots are the live
+    groups.  Returns bf16 out [T, hidden]."""
+    lib = load_library()
+    _cuda(x_fp8, "x_fp8", _FP8)
+    _cuda(x_scale, "x_scale", torch.int32)
+    T, n_slots, D = x_fp8.shape
+    if x_fp8.stride() != (D, T * D, 1):
+        raise ValueError("x_fp8 must be the [T, slots, D] view of a physical [slots, T, D] buffer")
+    PK = (D // 128 + 3) // 4
+    T_al = tma_aligned_tokens(T)
+    if T > 0 and (tuple(x_scale.shape) != (T, n_slots, PK) or
+                  x_scale.stride() != (1, PK * T_al, T_al)):
+        raise ValueError("x_scale must be the [T, slots, PK] view of a physical [slots, PK, T_al] "
+                         "buffer")
+    C = n_groups * o_lora_rank
+    hidden = _check_o_proj_weights(wo_a, wo_a_scale, wo_b, wo_b_scale, C, D)
+    need = dsv4_o_proj_prequant_workspace_bytes(T, n_groups, o_lora_rank)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x_fp8.device)
+    if out is None:
+        out = torch.empty((T, hidden), dtype=torch.bfloat16, device=x_fp8.device)
+    rc = lib.dsv4_o_proj_prequant(x_fp8.data_ptr(), x_scale.data_ptr(), T, n_slots, n_groups, D,
+                                  o_lora_rank, hidden, wo_a.data_ptr(), wo_a_scale.data_ptr(),
+                                  wo_b.data_ptr(), wo_b_scale.data_ptr(), out.data_ptr(),
+                                  workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check(rc, "dsv4_o_proj_prequant")
+    return out
+
+
+def prequant_workspace_views(workspace: torch.Tensor, num_tokens: int, n_groups: int,
+                             o_lora_rank: int) -> dict:
+    """zq uint8 [T, G*R] and zs int32 [PKC, T_al] inside dsv4_o_proj_prequant's workspace."""
+    T, C = num_tokens, n_groups * o_lora_rank
+    PKC = (C // 128 + 3) // 4
+    T_al = tma_aligned_tokens(T)
+    ws = workspace.view(torch.uint8)
+    zq = ws[:T * C].view(T, C)
+    off = _round256(T * C)
+    zs = ws[off:off + PKC * T_al * 4].view(torch.int32).view(PKC, T_al)
+    return {"zq": zq, "zs": zs}
+
+
+def static_scratch_bytes() -> int:
+    """Size of the library's own scratch for dsv4_o_proj_static (read from the library)."""
+    return int(load_library().dsv4_static_scratch_bytes())
 
 
 def dsv4_o_proj_static(o: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,

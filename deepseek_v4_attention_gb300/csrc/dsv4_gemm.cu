@@ -694,7 +694,20 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
           bulk_commit_group();
         }
       };
-      if constexpr (kEpi == kEpiBf16) {
+      if constexpr (kEpi == kEpiF32) {
+        // eight chunks of 16 columns (64 bytes of fp32 per row), the
+        // accumulators unchanged
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int b = 16 * (c & 1) + 4 * q;
+            v[q] = make_uint4(r[c >> 1][b], r[c >> 1][b + 1], r[c >> 1][b + 2], r[c >> 1][b + 3]);
+          }
+          stage_chunk(v, static_cast<int32_t>(col0 + 16 * c));
+        }
+      } else if constexpr (kEpi == kEpiBf16) {
         // four chunks of 32 columns (64 bytes of bf16 per row)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -817,15 +830,14 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   // library's (inside dsv4_o_proj), so the launch may overlap it: this kernel
   // reads only weights before griddep_wait().
   using C = Cfg<kBN, kARows, kFused>;
-  static int configured_for[64] = {0};
-  if (dev.device < 0 || dev.device >= 64) return DSV4_ERR_UNSUPPORTED;
-  if (!configured_for[dev.device]) {
-    if (cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows, kFused>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::smem_bytes)) != cudaSuccess)
-      return DSV4_ERR_CUDA;
-    configured_for[dev.device] = 1;
-  }
+  static std::atomic<int> configured_for[kMaxDevices];
+  if (dev.device < 0 || dev.device >= kMaxDevices) return DSV4_ERR_UNSUPPORTED;
+  const int configured = lazy_per_device(configured_for, dev.device, [] {
+    return cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows, kFused>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(C::smem_bytes)) == cudaSuccess ? 1 : 0;
+  });
+  if (!configured) return DSV4_ERR_CUDA;
   const int64_t T = q.T;
   const int64_t t_al = (T + 3) / 4 * 4;
   const int packs = (q.K / 128 + 3) / 4;
@@ -865,14 +877,20 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   }
   CUtensorMap tm_out;
   {
+    // rows of G*N elements; a box is 32 rows x 64 bytes (64 e4m3 codes, 32
+    // bf16 or 16 fp32 values)
     const int64_t ld = static_cast<int64_t>(q.G) * q.N;
-    const bool quant = kEpi == kEpiQuant;
-    const void* base = quant ? static_cast<const void*>(q.q_out) : q.out_bf16;
+    const int osz = kEpi == kEpiQuant ? 1 : kEpi == kEpiF32 ? 4 : 2;
+    const void* base = kEpi == kEpiQuant ? static_cast<const void*>(q.q_out)
+                       : kEpi == kEpiF32 ? static_cast<const void*>(q.out_f32)
+                                         : q.out_bf16;
+    const CUtensorMapDataType odt = kEpi == kEpiQuant ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                    : kEpi == kEpiF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(ld), static_cast<cuuint64_t>(T)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * (quant ? 1 : 2))};
-    cuuint32_t box[2] = {quant ? 64u : 32u, 32u};   // 64-byte rows
-    if (!encode(&tm_out, quant ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * osz)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / osz), 32u};
+    if (!encode(&tm_out, odt, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
       return DSV4_ERR_CUDA;
   }
   Params p;
@@ -931,6 +949,19 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
+// The FP8 tile paths for one epilogue.
+template <int kEpi>
+int launch_fp8(const GemmProblem& q, bool wide, bool small_m, bool split, cudaStream_t stream,
+               const DeviceInfo& dev) {
+  if (wide) return launch_impl<256, kEpi, 1, false, 128>(q, stream, dev);
+  if (small_m) {
+    if (split) return launch_impl<128, kEpi, 2, false, 64>(q, stream, dev);
+    return launch_impl<128, kEpi, 1, false, 64>(q, stream, dev);
+  }
+  if (split) return launch_impl<128, kEpi, 2, false, 128>(q, stream, dev);
+  return launch_impl<128, kEpi, 1, false, 128>(q, stream, dev);
+}
+
 }  // namespace
 
 int launch_block_scaled_gemm(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
@@ -938,7 +969,8 @@ int launch_block_scaled_gemm(const GemmProblem& q, cudaStream_t stream, const De
   if (q.fused_a) {
     // decode sizes only: one 64-row m-tile, 128-wide tiles, split over K when
     // both halves hold whole scale packs and the split still fits the GPU
-    if (q.bf16 || q.T > 64 || q.N % 128 != 0 || q.K != q.heads_per_group * 512)
+    if (q.bf16 || q.T > 64 || q.N % 128 != 0 || q.K != q.heads_per_group * 512 ||
+        q.epilogue == kEpiF32)
       return DSV4_ERR_UNSUPPORTED;
     const int64_t tiles = static_cast<int64_t>(q.N / 128) * q.G;
     const bool split = (q.K / 128) % 8 == 0 && 2 * tiles <= dev.num_sms;
@@ -972,24 +1004,11 @@ int launch_block_scaled_gemm(const GemmProblem& q, cudaStream_t stream, const De
     if (split) return launch_impl<128, kEpiBf16, 2, true, 128>(q, stream, dev);
     return launch_impl<128, kEpiBf16, 1, true, 128>(q, stream, dev);
   }
-  if (wide) {
-    if (q.epilogue == kEpiQuant) return launch_impl<256, kEpiQuant, 1, false, 128>(q, stream, dev);
-    return launch_impl<256, kEpiBf16, 1, false, 128>(q, stream, dev);
+  switch (q.epilogue) {
+    case kEpiQuant: return launch_fp8<kEpiQuant>(q, wide, small_m, split, stream, dev);
+    case kEpiF32: return launch_fp8<kEpiF32>(q, wide, small_m, split, stream, dev);
+    default: return launch_fp8<kEpiBf16>(q, wide, small_m, split, stream, dev);
   }
-  if (small_m) {
-    if (split) {
-      if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 2, false, 64>(q, stream, dev);
-      return launch_impl<128, kEpiBf16, 2, false, 64>(q, stream, dev);
-    }
-    if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 1, false, 64>(q, stream, dev);
-    return launch_impl<128, kEpiBf16, 1, false, 64>(q, stream, dev);
-  }
-  if (split) {
-    if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 2, false, 128>(q, stream, dev);
-    return launch_impl<128, kEpiBf16, 2, false, 128>(q, stream, dev);
-  }
-  if (q.epilogue == kEpiQuant) return launch_impl<128, kEpiQuant, 1, false, 128>(q, stream, dev);
-  return launch_impl<128, kEpiBf16, 1, false, 128>(q, stream, dev);
 }
 
 }  // namespace dsv4

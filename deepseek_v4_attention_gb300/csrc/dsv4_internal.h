@@ -6,7 +6,35 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace dsv4 {
+
+constexpr int kMaxDevices = 64;
+
+// Host state computed once per device on first use (a function attribute set,
+// an occupancy figure): thread-safe, and only a success is kept, so a failed
+// first attempt (a transient error, a call made during stream capture) is
+// retried by the next call instead of being remembered.  `compute` returns a
+// positive value on success.
+inline std::mutex& lazy_state_mutex() {
+  static std::mutex m;
+  return m;
+}
+
+template <class F>
+int lazy_per_device(std::atomic<int> (&slots)[kMaxDevices], int device, F compute) {
+  if (device < 0 || device >= kMaxDevices) return 0;
+  int v = slots[device].load(std::memory_order_acquire);
+  if (v > 0) return v;
+  std::lock_guard<std::mutex> lock(lazy_state_mutex());
+  v = slots[device].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  v = compute();
+  if (v > 0) slots[device].store(v, std::memory_order_release);
+  return v;
+}
 
 struct DeviceInfo {
   int device = -1;
@@ -21,6 +49,7 @@ struct DeviceInfo {
 enum GemmEpilogue : int {
   kEpiBf16 = 0,   // store fp32 accumulators as bf16 rows [T][G*N]
   kEpiQuant = 1,  // round to bf16, then per-128 UE8M0 FP8 re-quantisation of each row
+  kEpiF32 = 2,    // store the fp32 accumulators as they are, rows [T][G*N]
 };
 
 struct GemmProblem {
@@ -48,6 +77,7 @@ struct GemmProblem {
   int heads = 0;                    // G * heads_per_group
   int heads_per_group = 0;
   void* out_bf16 = nullptr;         // bf16 [T][G*N] (kEpiBf16)
+  float* out_f32 = nullptr;         // fp32 [T][G*N] (kEpiF32)
   uint8_t* q_out = nullptr;         // e4m3 [T][G*N]           (kEpiQuant)
   int32_t* q_scale = nullptr;       // int32 [ceil(G*N/512)][T_al] (kEpiQuant)
 };
@@ -63,5 +93,9 @@ int launch_inv_rope_bf16(const void* o, const int64_t* positions, const float* c
                          const DeviceInfo& dev);
 
 int launch_block_scaled_gemm(const GemmProblem& p, cudaStream_t stream, const DeviceInfo& dev);
+
+// out[i] = bf16(sum over j < n of parts[j][i]), summed in fp32 in the order j = 0, 1, ...
+int launch_sum_partials(const float* const* parts, int n, int64_t elems, void* out_bf16,
+                        cudaStream_t stream, const DeviceInfo& dev);
 
 }  // namespace dsv4

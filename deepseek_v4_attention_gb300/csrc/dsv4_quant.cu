@@ -193,13 +193,13 @@ void launch_bf16_u(const void* o, const int64_t* positions, const float* cache, 
   int64_t blocks = (items * 32 + threads - 1) / threads;
   // one wave: as many blocks as are resident at once (the registers bound it;
   // a second, partial wave of blocks measured 2-3 % slower)
-  static int resident[64] = {0};
-  int& per_sm = resident[dev.device >= 0 && dev.device < 64 ? dev.device : 0];
-  if (per_sm == 0 &&
-      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, inv_rope_bf16_kernel<kU>, threads,
-                                                     0) != cudaSuccess ||
-       per_sm <= 0))
-    per_sm = 2048 / threads;
+  static std::atomic<int> resident[kMaxDevices];
+  int per_sm = lazy_per_device(resident, dev.device, [&] {
+    int n = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, inv_rope_bf16_kernel<kU>, threads, 0) ==
+                   cudaSuccess ? n : 0;
+  });
+  if (per_sm <= 0) per_sm = 2048 / threads;   // not known: a full SM's worth
   const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * per_sm;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
@@ -218,13 +218,13 @@ void launch_u(const void* o, const int64_t* positions, const float* cache, int64
   int64_t blocks = (items * 32 + threads - 1) / threads;
   // one wave: as many blocks as are resident at once (the registers bound it;
   // a second, partial wave of blocks measured 2-3 % slower)
-  static int resident[64] = {0};
-  int& per_sm = resident[dev.device >= 0 && dev.device < 64 ? dev.device : 0];
-  if (per_sm == 0 &&
-      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, inv_rope_fp8_quant_kernel<kU>, threads,
-                                                     0) != cudaSuccess ||
-       per_sm <= 0))
-    per_sm = 2048 / threads;
+  static std::atomic<int> resident[kMaxDevices];
+  int per_sm = lazy_per_device(resident, dev.device, [&] {
+    int n = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, inv_rope_fp8_quant_kernel<kU>, threads, 0) ==
+                   cudaSuccess ? n : 0;
+  });
+  if (per_sm <= 0) per_sm = 2048 / threads;   // not known: a full SM's worth
   const int64_t max_blocks = static_cast<int64_t>(dev.num_sms) * per_sm;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;

@@ -4,6 +4,7 @@
 // that dsv4_o_proj takes from its caller lives here instead, in one file-scope
 // device array of DSV4_STATIC_SCRATCH_BYTES that every device loading this
 // library holds until the process exits.  Nothing here allocates.
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -16,23 +17,27 @@ namespace {
 // the symbol, not a device address: kernels get the address looked up below.
 static __device__ __align__(256) uint8_t g_o_proj_scratch[DSV4_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::once_flag g_setup_once[kMaxDevices];
-void* g_scratch_addr[kMaxDevices];
-int g_setup_rc[kMaxDevices];
+// The device address of the array, looked up once per device with that device
+// current.  Only a successful lookup is kept; a failed one (say a first call
+// made during stream capture) is tried again by the next call.
+std::mutex g_setup_mutex;
+std::atomic<bool> g_scratch_ready[dsv4::kMaxDevices];
+void* g_scratch_addr[dsv4::kMaxDevices];
 
-// Once per device, with that device current: the device address of the array.
 int scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return DSV4_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return DSV4_ERR_UNSUPPORTED;
-  std::call_once(g_setup_once[dev], [dev] {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_o_proj_scratch);
-    g_setup_rc[dev] = (e == cudaSuccess && p != nullptr) ? DSV4_OK : DSV4_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  });
-  if (g_setup_rc[dev] != DSV4_OK) return g_setup_rc[dev];
+  if (dev < 0 || dev >= dsv4::kMaxDevices) return DSV4_ERR_UNSUPPORTED;
+  if (!g_scratch_ready[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_ready[dev].load(std::memory_order_relaxed)) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_o_proj_scratch) != cudaSuccess || p == nullptr)
+        return DSV4_ERR_CUDA;
+      g_scratch_addr[dev] = p;
+      g_scratch_ready[dev].store(true, std::memory_order_release);
+    }
+  }
   *out = g_scratch_addr[dev];
   return DSV4_OK;
 }
@@ -64,3 +69,5 @@ extern "C" int dsv4_o_proj_static(const void* o, const int64_t* positions,
                                  o_lora_rank, hidden, wo_a_fp8, wo_a_scale, wo_b_fp8, wo_b_scale,
                                  out, scratch, DSV4_STATIC_SCRATCH_BYTES, nullptr, stream);
 }
+
+extern "C" size_t dsv4_static_scratch_bytes(void) { return DSV4_STATIC_SCRATCH_BYTES; }

@@ -88,8 +88,8 @@ WORKLOADS = {
 }
 
 
-def _gen(seed: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def _gen(seed: int, device: torch.device | str = "cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(seed)
     return g
 
@@ -102,25 +102,31 @@ def cos_sin_cache(max_pos: int, rope_dim: int = 64, theta: float = ROPE_THETA) -
     return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32).contiguous()
 
 
-def attention_output(w: Workload, gen: torch.Generator | None = None) -> torch.Tensor:
-    """bf16 o [T, H, head_dim] with the workload's value distribution."""
-    gen = gen or _gen(w.seed)
+def attention_output(w: Workload, gen: torch.Generator | None = None,
+                     device: torch.device | str = "cpu") -> torch.Tensor:
+    """bf16 o [T, H, head_dim] with the workload's value distribution, drawn on
+    `device` (with a CPU generator by default; on another device the same
+    recipe runs on that device's random stream, so the values differ)."""
+    gen = gen or _gen(w.seed, device)
     shape = (w.T, w.H, w.head_dim)
     if w.dist == "normal":
-        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        x = torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
     elif w.dist == "outliers":
-        x = torch.randn(shape, generator=gen, dtype=torch.float32)
-        hit = torch.rand(shape, generator=gen) < 0.01
+        x = torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+        hit = torch.rand(shape, generator=gen, device=device) < 0.01
         x = torch.where(hit, x * 50.0, x)
     elif w.dist == "student_t":
-        z = torch.randn(shape, generator=gen, dtype=torch.float32)
-        chi2 = torch.randn((3,) + shape, generator=gen, dtype=torch.float32).square().sum(0)
+        z = torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+        chi2 = torch.zeros(shape, dtype=torch.float32, device=device)
+        for _ in range(3):
+            chi2 += torch.randn(shape, generator=gen, dtype=torch.float32, device=device).square()
         x = z / torch.sqrt(chi2 / 3.0)
+        del chi2
         qgs = w.quant_group_size
         blocks = x.view(w.T * w.H * (w.head_dim // qgs), qgs)
         nblk = blocks.shape[0]
         nzero = max(1, round(nblk * 0.001))
-        idx = torch.randperm(nblk, generator=gen)[:nzero]
+        idx = torch.randperm(nblk, generator=gen, device=device)[:nzero]
         blocks[idx] = 0.0
     else:
         raise ValueError(w.dist)
@@ -156,11 +162,14 @@ def bf16_weight(rows: int, cols: int, seed: int) -> torch.Tensor:
         torch.bfloat16).contiguous()
 
 
-def make_inputs(w: Workload, with_wo_b: bool = True) -> dict:
-    """All CPU tensors of one workload: o, positions, cache, wo_a (+ wo_b)."""
-    gen = _gen(w.seed)
+def make_inputs(w: Workload, with_wo_b: bool = True,
+                o_device: torch.device | str | None = None) -> dict:
+    """All tensors of one workload: o, positions, cache, wo_a (+ wo_b), on the
+    CPU; with o_device, o is drawn on that device instead (same recipe, that
+    device's random stream)."""
+    gen = _gen(w.seed) if o_device is None else _gen(w.seed, o_device)
     d = {
-        "o": attention_output(w, gen),
+        "o": attention_output(w, gen, "cpu" if o_device is None else o_device),
         "positions": positions(w),
         "cache": cos_sin_cache(w.max_pos, w.rope_dim),
     }

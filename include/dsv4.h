@@ -179,10 +179,20 @@ int dsv4_grouped_wo_a_bf16(const void* x_bf16, int64_t num_tokens, int n_groups,
                            int o_lora_rank, const void* w_bf16, void* z, void* stream);
 
 /*
- * Bytes of caller-owned scratch that dsv4_o_proj needs for these sizes: the
- * quantised groups x [G][T][D] with their scales [G][PK][T_al], and the
- * per-128 re-quantised z [T][G*R] with its scales [G*R/512][T_al] (each part
- * 256-byte aligned).  Returns 0 for invalid sizes.
+ * Bytes of caller-owned scratch that dsv4_o_proj needs for these sizes.
+ * Returns 0 for invalid sizes.  The workspace holds four parts, in this order,
+ * each starting at the previous part's end rounded up to a multiple of 256
+ * bytes (the first at offset 0):
+ *   x   e4m3 codes of the quantised groups, physical [G][T][D]
+ *   xs  their packed UE8M0 scales, int32 physical [G][PK][T_al]
+ *   zq  e4m3 codes of the per-128 re-quantised bf16 z, [T][G*R] row-major
+ *   zs  their packed UE8M0 scales, int32 physical [ceil(G*R/512)][T_al]
+ *       (byte c/128 % 4 of word c/512 of token t for 128-column block c/128;
+ *       when G*R/128 is not a multiple of 4 the last word's unused high
+ *       bytes are unspecified)
+ * After dsv4_o_proj returns and its kernels have run, these parts hold the
+ * call's intermediate results (pad columns [T, T_al) of the scales are
+ * unspecified); a caller may read them, e.g. to check each stage.
  */
 size_t dsv4_o_proj_workspace_bytes(int64_t num_tokens, int n_groups, int heads_per_group,
                                    int head_dim, int o_lora_rank);
@@ -276,6 +286,116 @@ int dsv4_o_proj_static(const void* o, const int64_t* positions, const float* cos
                        int hidden, const void* wo_a_fp8, const uint8_t* wo_a_scale,
                        const void* wo_b_fp8, const uint8_t* wo_b_scale, void* out,
                        void* stream);
+
+/* DSV4_STATIC_SCRATCH_BYTES as this library was built with it (so that a
+ * caller or a binding compiled separately can check its own copy). */
+size_t dsv4_static_scratch_bytes(void);
+
+/*
+ * Eligibility of a layer for a pre-quantised attention output (vLLM docs,
+ * o_proj page, rope_quant_unsupported_reason): an attention kernel may emit o
+ * already inverse-rotated and cast to FP8 in the RopeQuant layout
+ * (rope_quant_attn_out: DSV4_ROPE_QUANT_NUM_HEADS heads as
+ * DSV4_ROPE_QUANT_NUM_HEADS / DSV4_ROPE_QUANT_HEADS_PER_GROUP group slots of
+ * DSV4_ROPE_QUANT_HEADS_PER_GROUP heads x 512) only when the layer has exactly
+ * that many local query heads, the per-tensor FP8 KV cache and an FP8 wo_a.
+ *
+ *   n_local_heads  query heads of the layer on this rank
+ *   kv_cache_fp8   non-zero if the KV cache is per-tensor FP8 (e4m3)
+ *   wo_a_fp8       non-zero if wo_a's weight is FP8 (e4m3)
+ *   reason         if not NULL, receives NULL (eligible) or a static string
+ *                  saying why not
+ *
+ * Returns DSV4_OK or DSV4_ERR_UNSUPPORTED.  Host only; no CUDA call.
+ */
+#define DSV4_ROPE_QUANT_NUM_HEADS 128
+#define DSV4_ROPE_QUANT_HEADS_PER_GROUP 8
+int dsv4_rope_quant_unsupported_reason(int n_local_heads, int kv_cache_fp8, int wo_a_fp8,
+                                       const char** reason);
+
+/*
+ * Scratch bytes of dsv4_o_proj_prequant: the re-quantised z [T][G*R] e4m3 at
+ * offset 0, then its packed scales int32 [ceil(G*R/512)][T_al] at the next
+ * 256-byte boundary.  Returns 0 for invalid sizes.
+ */
+size_t dsv4_o_proj_prequant_workspace_bytes(int64_t num_tokens, int n_groups, int o_lora_rank);
+
+/*
+ * The O-projection from a pre-quantised attention output (vLLM docs, o_proj
+ * page, deep_gemm_fp8_o_proj with a QuantizedActivation o): the attention
+ * kernel already inverse-rotated o and cast it to FP8, one wo_a group per
+ * slot with the live groups first, so only the padding slots are left out
+ * (o.data[:, :n_groups], o.scale[:, :n_groups]) before the grouped wo_a,
+ * the fused per-128 re-quantisation of the bf16 z and wo_b.  Two launches.
+ *
+ *   x_fp8    device e4m3, physical [n_slots][T][group_dim] (the [T, n_slots,
+ *            group_dim] view with strides (group_dim, T*group_dim, 1))
+ *   x_scale  device int32, physical [n_slots][PK][T_al], PK = ceil(group_dim/512)
+ *            (the [T, n_slots, PK] view with strides (1, PK*T_al, T_al));
+ *            slots >= n_groups are never read
+ *   n_slots  group slots of the buffers (16 for the RopeQuant layout)
+ *   n_groups live groups, <= n_slots
+ *   wo_a_fp8, wo_a_scale, wo_b_fp8, wo_b_scale, out: as dsv4_o_proj
+ *   workspace at least dsv4_o_proj_prequant_workspace_bytes(), 256-byte aligned
+ *
+ * Errors: DSV4_ERR_SHAPE unless group_dim, o_lora_rank and hidden are positive
+ * multiples of 128 and 0 < n_groups <= n_slots; DSV4_ERR_NULL / DSV4_ERR_ALIGN
+ * (16 bytes; the workspace 256) / DSV4_ERR_WORKSPACE as dsv4_o_proj.  Whether
+ * a layer may take this path is dsv4_rope_quant_unsupported_reason()'s answer.
+ */
+int dsv4_o_proj_prequant(const void* x_fp8, const int32_t* x_scale, int64_t num_tokens,
+                         int n_slots, int n_groups, int group_dim, int o_lora_rank, int hidden,
+                         const void* wo_a_fp8, const uint8_t* wo_a_scale, const void* wo_b_fp8,
+                         const uint8_t* wo_b_scale, void* out, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
+ * One rank's share of group-split tensor parallelism (sglang deepseek_v4.py,
+ * the column-parallel wo_a and row-parallel wo_b of the attention layer, with
+ * attn_tp_all_reduce after wo_b; vLLM docs, o_proj page, wo_b as "a wrapper
+ * that also reduce-scatters its output (DeepSeek-V4.1 GEMM-RS)").  The rank
+ * owns the groups [g0, g0 + n_groups) of the layer: their heads of o, their
+ * wo_a rows and the matching wo_b columns.  Because group g's z meets only
+ * wo_b columns g*R .. (g+1)*R - 1 and the per-128 re-quantisation of z never
+ * crosses a group, the rank's part of out is dsv4_o_proj over its own groups,
+ * and out is the sum of the parts over all ranks.  This call writes that part
+ * unrounded, in fp32, so that the sum rounds to bf16 once
+ * (dsv4_sum_partials).
+ *
+ *   o              device bf16 [T, n_groups*heads_per_group, 512]: the rank's heads
+ *   wo_a_fp8       device e4m3 [n_groups*R, D]: rows g0*R .. (g0+n_groups)*R - 1
+ *   wo_a_scale     device UE8M0 [n_groups*R/128, D/128]
+ *   wo_b_fp8       device e4m3 [hidden, n_groups*R]: columns g0*R .. of the layer's
+ *                  wo_b, stored contiguously
+ *   wo_b_scale     device UE8M0 [hidden/128, n_groups*R/128]
+ *   out_partial    device fp32 [T, hidden]
+ *   other arguments, workspace and errors: as dsv4_o_proj
+ */
+int dsv4_o_proj_partial(const void* o, const int64_t* positions, const float* cos_sin_cache,
+                        int64_t max_pos, int64_t num_tokens, int n_groups, int heads_per_group,
+                        int nope_dim, int rope_dim, int quant_group_size, int o_lora_rank,
+                        int hidden, const void* wo_a_fp8, const uint8_t* wo_a_scale,
+                        const void* wo_b_fp8, const uint8_t* wo_b_scale, float* out_partial,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Most partial outputs dsv4_sum_partials adds in one call. */
+#define DSV4_MAX_PARTIALS 16
+
+/*
+ * out[i] = bf16(parts[0][i] + parts[1][i] + ... + parts[n-1][i]), summed in
+ * fp32 in that order, rounded to nearest even: the partial outputs of
+ * dsv4_o_proj_partial added into the layer's output (n > 1, all on this
+ * device), or, with n = 1, the conversion of an fp32 reduce-scatter's result.
+ *
+ *   partials    HOST array of n device pointers, each fp32 [num_elems], 16-byte aligned
+ *   n_partials  1 .. DSV4_MAX_PARTIALS
+ *   out_bf16    device bf16 [num_elems], 16-byte aligned; may not overlap a partial
+ *
+ * Errors: DSV4_ERR_SHAPE for n out of range or num_elems < 0, DSV4_ERR_NULL,
+ * DSV4_ERR_ALIGN.
+ */
+int dsv4_sum_partials(const float* const* partials, int n_partials, int64_t num_elems,
+                      void* out_bf16, void* stream);
 
 /* Human-readable name of a dsv4_status value (static string). */
 const char* dsv4_status_string(int status);

@@ -22,7 +22,10 @@ def test_exports_every_header_function(lib):
                           "dsv4_o_proj_workspace_bytes", "dsv4_o_proj", "dsv4_o_proj_with_events",
                           "dsv4_o_proj_static", "dsv4_selftest_wait_timeout",
                           "dsv4_inv_rope_bf16", "dsv4_grouped_wo_a_bf16",
-                          "dsv4_inv_rope_grouped_wo_a",
+                          "dsv4_inv_rope_grouped_wo_a", "dsv4_static_scratch_bytes",
+                          "dsv4_o_proj_partial", "dsv4_sum_partials",
+                          "dsv4_rope_quant_unsupported_reason",
+                          "dsv4_o_proj_prequant_workspace_bytes", "dsv4_o_proj_prequant",
                           "dsv4_status_string",
                           "dsv4_device_status", "dsv4_last_launch_count"}
     out = subprocess.run(["nm", "-D", "--defined-only", k.LIB_PATH], capture_output=True,
@@ -167,3 +170,57 @@ def test_bf16_entries_host_validation_without_gpu(lib):
     assert g(*a) == -2
     a = list(good); a[6] = P + 2
     assert g(*a) == -3
+
+
+def test_rope_quant_eligibility(lib):
+    """rope_quant_unsupported_reason of the o_proj page: 128 local heads, the
+    per-tensor FP8 KV cache and an FP8 wo_a, checked in that order."""
+    assert k.rope_quant_unsupported_reason(128, True, True) is None
+    assert "128" in k.rope_quant_unsupported_reason(64, True, True)
+    assert "128" in k.rope_quant_unsupported_reason(256, False, False)
+    assert "KV" in k.rope_quant_unsupported_reason(128, False, True)
+    assert "wo_a" in k.rope_quant_unsupported_reason(128, True, False)
+    assert lib.dsv4_rope_quant_unsupported_reason(128, 1, 1, None) == 0
+    assert lib.dsv4_rope_quant_unsupported_reason(96, 1, 1, None) == -4
+    assert k.ROPE_QUANT_NUM_HEADS == 128 and k.ROPE_QUANT_HEADS_PER_GROUP == 8
+
+
+def test_static_scratch_size_matches_header(lib):
+    import re
+    with open(k.HEADER) as f:
+        m = re.search(r"#define DSV4_STATIC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)",
+                      f.read())
+    assert m and k.static_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+
+
+def test_prequant_and_partial_host_validation_without_gpu(lib):
+    P = 4096
+    T, slots, G, D, R, hidden = 8, 16, 12, 4096, 1024, 7168
+    need = k.dsv4_o_proj_prequant_workspace_bytes(T, G, R)
+    pkc, t_al = (G * R // 128 + 3) // 4, 8
+    assert need == 256 * (-(-T * G * R // 256)) + 256 * (-(-pkc * t_al * 4 // 256))
+    assert k.dsv4_o_proj_prequant_workspace_bytes(T, G, 100) == 0
+    f = lib.dsv4_o_proj_prequant
+    good = [P, P, T, slots, G, D, R, hidden, P, P, P, P, P, P, need, None]
+    for idx, val, rc in [(2, -1, -1), (4, 0, -1), (4, 17, -1), (5, 4000, -1), (6, 1000, -1),
+                         (7, 7000, -1), (14, need - 1, -5), (13, P + 16, -3)]:
+        a = list(good); a[idx] = val
+        assert f(*a) == rc, (idx, val)
+    a = list(good); a[2] = 0; a[0] = None
+    assert f(*a) == 0 and k.dsv4_last_launch_count() == 0
+    for idx in (0, 1, 8, 9, 10, 11, 12):
+        a = list(good); a[idx] = None
+        assert f(*a) == -2, idx
+    for idx in (0, 1, 8, 10, 12):
+        a = list(good); a[idx] = P + 8
+        assert f(*a) == -3, idx
+    g = lib.dsv4_o_proj_partial
+    wsz = k.dsv4_o_proj_workspace_bytes(T, 8, 8, 512, R)
+    good = [P, P, P, 65536, T, 8, 8, 448, 64, 128, R, hidden, P, P, P, P, P, P, wsz, None]
+    assert g(*[*good[:11], 100, *good[12:]]) == -1                 # hidden % 128
+    a = list(good); a[16] = None
+    assert g(*a) == -2
+    a = list(good); a[18] = wsz - 1
+    assert g(*a) == -5
+    a = list(good); a[4] = 0
+    assert g(*a) == 0 and k.dsv4_last_launch_count() == 0

@@ -6,7 +6,7 @@ import torch
 
 import dsv4_inputs as di
 import oracle
-from gpu_helpers import (GEMM_RTOL, assert_chain_matches, assert_codes_match, cuda_or_skip,
+from gpu_helpers import (GEMM_RTOL, assert_codes_match, check_o_proj_parts, cuda_or_skip,
                          gemm_rel_err, to_bits)
 
 pytestmark = pytest.mark.gpu
@@ -93,7 +93,7 @@ def test_grouped_wo_a_decode_config_parity(dev):
 
 def test_grouped_wo_a_prefill_config_sampled(dev):
     """T = 8192 prefill workload (all groups, all columns) checked on a seeded
-    sample of 256 token rows (the product is row-independent)."""
+    sample of 512 token rows (the product is row-independent)."""
     import deepseek_v4_attention_gb300 as k
     w = di.WORKLOADS["prefill"]
     d = di.make_inputs(w, with_wo_b=False)
@@ -103,59 +103,67 @@ def test_grouped_wo_a_prefill_config_sampled(dev):
                             w.o_lora_rank)
     torch.cuda.synchronize()
     assert k.dsv4_device_status(clear=True) == 0
-    idx = np.sort(np.random.default_rng(0).choice(w.T, 256, replace=False))
+    idx = np.sort(np.random.default_rng(0).choice(w.T, 512, replace=False))
     ti = torch.from_numpy(idx)
     xr, xsr = oracle.inv_rope_fp8_quant(d["o"][ti], d["positions"][ti], d["cache"], w.n_groups,
                                         w.heads_per_group)
     # the GPU's own quantised rows are what its GEMM consumed; they match the oracle's
     qg = to_bits(q.view(torch.uint8).transpose(0, 1))[:, idx]
     assert_codes_match(qg, xr)
-    _, z64 = oracle.grouped_gemm(xr, xsr, d["wo_a"], d["wo_a_scale"], len(idx), w.n_groups, w.D,
-                                 w.o_lora_rank, want_fp64=True)
+    sg = s.permute(1, 2, 0).cpu().numpy()[:, :, idx]
+    assert np.array_equal(sg, xsr[:, :, :len(idx)])
+    _, z64 = oracle.grouped_gemm(np.ascontiguousarray(qg), xsr, d["wo_a"], d["wo_a_scale"],
+                                 len(idx), w.n_groups, w.D, w.o_lora_rank, want_fp64=True)
     zg = to_bits(z)[idx]
     assert gemm_rel_err(zg, z64) <= GEMM_RTOL
 
 
-def _o_proj_gpu(d, w, dev, T=None):
+def _o_proj_gpu(d, w, dev):
+    """dsv4_o_proj with a caller workspace; returns (out, workspace) on the device."""
     import deepseek_v4_attention_gb300 as k
+    need = k.dsv4_o_proj_workspace_bytes(w.T, w.n_groups, w.heads_per_group, w.head_dim,
+                                         w.o_lora_rank)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
     out = k.dsv4_o_proj(d["o"].to(dev), d["positions"].to(dev), d["cache"].to(dev),
                         d["wo_a"].to(dev), d["wo_a_scale"].to(dev), d["wo_b"].to(dev),
                         d["wo_b_scale"].to(dev), n_groups=w.n_groups,
-                        heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank)
+                        heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank,
+                        workspace=ws)
     assert k.dsv4_last_launch_count() == 3
     torch.cuda.synchronize()
     assert k.dsv4_device_status(clear=True) == 0
-    return to_bits(out)
+    return out, ws
 
 
 @pytest.mark.parametrize("T", [16, 1, 5, 131])
 def test_o_proj_tiny_parity(dev, T):
     w = di.WORKLOADS["tiny"].with_tokens(T, seed=T)
     d = di.make_inputs(w)
-    og = _o_proj_gpu(d, w, dev)
-    _, out64, _ = oracle.o_proj(d["o"], d["positions"], d["cache"], d["wo_a"], d["wo_a_scale"],
-                                d["wo_b"], d["wo_b_scale"], n_groups=w.n_groups,
-                                heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank,
-                                hidden=w.hidden)
-    assert_chain_matches(og, out64)
+    out, ws = _o_proj_gpu(d, w, dev)
+    check_o_proj_parts(d, w, out, ws)
+
+
+def test_o_proj_decode_config_parity(dev):
+    """The decode workload (T = 64, 8 groups, hidden 7168) through the whole
+    chain, every row checked stage by stage."""
+    w = di.WORKLOADS["decode"]
+    d = di.make_inputs(w)
+    out, ws = _o_proj_gpu(d, w, dev)
+    check_o_proj_parts(d, w, out, ws)
 
 
 def test_o_proj_full_config_sampled(dev):
     """Full workload (T=4096, 128 heads, R=1024, hidden 7168) in the launch
-    configuration the benchmark times; 24 seeded token rows checked against the
-    oracle's whole chain (the path is row-independent)."""
+    configuration the benchmark times; 512 seeded token rows checked stage by
+    stage: the quantised groups, zq and its scales against the oracle, wo_b
+    against the fp64 product of the GPU's own zq (the path is row-independent)."""
     w = di.WORKLOADS["full"]
     d = di.make_inputs(w)
-    og = _o_proj_gpu(d, w, dev)
-    idx = np.sort(np.random.default_rng(1).choice(w.T, 24, replace=False))
-    ti = torch.from_numpy(idx)
-    _, out64, _ = oracle.o_proj(d["o"][ti], d["positions"][ti], d["cache"], d["wo_a"],
-                                d["wo_a_scale"], d["wo_b"], d["wo_b_scale"], n_groups=w.n_groups,
-                                heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank,
-                                hidden=w.hidden)
-    assert_chain_matches(og[idx], out64)
-    og2 = _o_proj_gpu(d, w, dev)
-    assert np.array_equal(og, og2), "two runs differ"
+    out, ws = _o_proj_gpu(d, w, dev)
+    idx = np.sort(np.random.default_rng(1).choice(w.T, 512, replace=False))
+    check_o_proj_parts(d, w, out, ws, idx)
+    out2, _ = _o_proj_gpu(d, w, dev)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16)), "two runs differ"
 
 
 @pytest.mark.parametrize("name,T", [("decode", 64), ("decode", 7), ("full", 300)])
@@ -165,9 +173,9 @@ def test_o_proj_deterministic(dev, name, T):
     A box, T = 300 the programmatically launched GEMMs."""
     w = di.WORKLOADS[name].with_tokens(T, seed=T + 11)
     d = di.make_inputs(w)
-    og = _o_proj_gpu(d, w, dev)
-    og2 = _o_proj_gpu(d, w, dev)
-    assert np.array_equal(og, og2), "two runs differ"
+    og, _ = _o_proj_gpu(d, w, dev)
+    og2, _ = _o_proj_gpu(d, w, dev)
+    assert torch.equal(og.view(torch.int16), og2.view(torch.int16)), "two runs differ"
 
 
 def test_o_proj_errors(dev):
@@ -297,12 +305,8 @@ def test_o_proj_random_shapes(dev, i):
     split-K, 64-row A box, ragged T) against the oracle's whole chain."""
     w = _random_o_proj_case(i)
     d = di.make_inputs(w)
-    og = _o_proj_gpu(d, w, dev)
-    _, out64, _ = oracle.o_proj(d["o"], d["positions"], d["cache"], d["wo_a"], d["wo_a_scale"],
-                                d["wo_b"], d["wo_b_scale"], n_groups=w.n_groups,
-                                heads_per_group=w.heads_per_group, o_lora_rank=w.o_lora_rank,
-                                hidden=w.hidden)
-    assert_chain_matches(og, out64, what=str(w))
+    out, ws = _o_proj_gpu(d, w, dev)
+    check_o_proj_parts(d, w, out, ws)
 
 
 # ---------------------------------------------------------------------------

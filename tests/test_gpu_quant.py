@@ -81,7 +81,7 @@ def test_quant_parity_prefill_outliers(dev):
 
 @pytest.mark.parametrize("name", ["quant8k", "quant32k"])
 def test_quant_parity_sweep_sampled(dev, name):
-    _compare(di.WORKLOADS[name], dev, sample_tokens=384)
+    _compare(di.WORKLOADS[name], dev, sample_tokens=512)
 
 
 def test_quant_position_zero_and_max(dev):

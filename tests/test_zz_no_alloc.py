@@ -52,11 +52,31 @@ def test_static_rejects_sizes_beyond_its_scratch(dev):
     import deepseek_v4_attention_gb300 as k
     lib = k.load_library()
     w = di.WORKLOADS["full"].with_tokens(813)       # 82.5 KB/token: one token too many
-    assert k.dsv4_o_proj_workspace_bytes(813, 16, 8, 512, 1024) > k.STATIC_SCRATCH_BYTES
-    assert k.dsv4_o_proj_workspace_bytes(812, 16, 8, 512, 1024) <= k.STATIC_SCRATCH_BYTES
+    assert k.dsv4_o_proj_workspace_bytes(813, 16, 8, 512, 1024) > k.static_scratch_bytes()
+    assert k.dsv4_o_proj_workspace_bytes(812, 16, 8, 512, 1024) <= k.static_scratch_bytes()
     d = {n: t.to(dev) for n, t in di.make_inputs(w).items()}
     out = torch.zeros((w.T, w.hidden), dtype=torch.bfloat16, device=dev)
     assert _static_call(lib, d, w, out) == k._NAME_TO_CODE["DSV4_ERR_WORKSPACE"]
     assert k.dsv4_last_launch_count() == 0
     torch.cuda.synchronize()
     assert bool((out == 0).all())          # nothing was written
+
+
+def test_static_calls_allocate_nothing(dev):
+    """After a first call (which looks up the scratch's device address), further
+    calls change neither the device's free memory nor torch's allocations."""
+    import deepseek_v4_attention_gb300 as k
+    lib = k.load_library()
+    w = di.WORKLOADS["full"].with_tokens(128, seed=9)
+    d = {n: t.to(dev) for n, t in di.make_inputs(w).items()}
+    out = torch.empty((w.T, w.hidden), dtype=torch.bfloat16, device=dev)
+    assert _static_call(lib, d, w, out) == 0
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(dev)
+    alloc0 = torch.cuda.memory_allocated(dev)
+    for _ in range(5):
+        assert _static_call(lib, d, w, out) == 0
+    torch.cuda.synchronize()
+    assert k.dsv4_device_status(clear=True) == 0
+    assert torch.cuda.mem_get_info(dev)[0] == free0
+    assert torch.cuda.memory_allocated(dev) == alloc0
