@@ -112,69 +112,111 @@ def config_of(w: di.Workload, n_gpus: int) -> dict:
 
 # ---------------------------------------------------------------- clocks --
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every INTERVAL_MS while the
-    `with` block runs.  The block starts only once the sampler has produced its
-    first sample (taken before the timed region, and not counted)."""
+    """SM clock, power and clock-event reasons of one GPU sampled every
+    INTERVAL_MS while the `with` block (the timed region) runs: read through
+    NVML (the library nvidia-smi itself uses) from a background thread, or,
+    where NVML cannot be loaded, by an nvidia-smi loop.  Nothing is set, only
+    read."""
+    INTERVAL_MS = 2
+    # clock-event reason bits of NVML's public API
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-    INTERVAL_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+        self.samples = []          # (sm_mhz, power_w or None, reason names)
+        self.max_mhz = None
+        self.source = None
+        self._nvml = None
+        self._thread = None
+        self._proc = None
+
+    def _nvml_handle(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit")
+        p = torch.cuda.get_device_properties(self.gpu)
+        bus = "%08x:%02x:%02x.0" % (getattr(p, "pci_domain_id", 0), getattr(p, "pci_bus_id", 0),
+                                    getattr(p, "pci_device_id", 0))
+        h = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+                raise OSError("nvml handle")
+        reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return nv, h, reasons
 
     def __enter__(self):
+        import ctypes
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
-        self.pre_taken = False
-        if self.proc is not None:
-            import select
-            ready, _, _ = select.select([self.proc.stdout], [], [], 3.0)
-            if ready:
-                self.proc.stdout.readline()          # the sample before the region
-                self.pre_taken = True
+            nv, h, reasons = self._nvml_handle()
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # 1: SM clock
+                self.max_mhz = float(mx.value)
+            self._stop = threading.Event()
+
+            def loop():
+                mhz, mw, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self._stop.is_set():
+                    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+                        pw = mw.value / 1e3 if nv.nvmlDeviceGetPowerUsage(
+                            h, ctypes.byref(mw)) == 0 else None
+                        rs = [n for b, n in self.REASONS.items() if bits.value & b] \
+                            if reasons(h, ctypes.byref(bits)) == 0 else []
+                        self.samples.append((float(mhz.value), pw, rs))
+                    self._stop.wait(self.INTERVAL_MS / 1e3)
+
+            self._thread = threading.Thread(target=loop, daemon=True)
+            self._thread.start()
+            self.source = f"nvml, every {self.INTERVAL_MS} ms"
+        except (OSError, AttributeError):
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi, every 20 ms"
+            except OSError:
+                self._proc = None
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                out, _ = self._proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
-            if not self.pre_taken:
-                self.lines = self.lines[1:]          # the sample before the region
+                self._proc.kill()
+                out, _ = self._proc.communicate()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for ln in out.splitlines():
+                f = [x.strip() for x in ln.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm, self.max_mhz = float(f[1]), float(f[2])
+                    pw = float(f[3])
+                except ValueError:
+                    continue
+                self.samples.append((sm, pw, [n for n, v in zip(names, f[5:9])
+                                              if v.lower().startswith("active")]))
 
     def summary(self) -> dict:
-        sm, mx, power, reasons = [], None, [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-                power.append(float(f[3]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None,
-                "interval_ms": self.INTERVAL_MS}
+        sm = [s[0] for s in self.samples]
+        pw = [s[1] for s in self.samples if s[1] is not None]
+        reasons = sorted({r for s in self.samples for r in s[2]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(sm),
+                "sm_mhz_min": min(sm) if sm else None,
+                "power_w_max": max(pw) if pw else None, "source": self.source}
 
 
 def recorded_traffic(kernel: str) -> float | None:
@@ -735,7 +777,11 @@ def run_workload(name: str, steps: int, warmup: int, local: int) -> dict:
                                          w.heads_per_group, out_fp8=st["x"], out_scale=st["xs"],
                                          stream=stream)
 
-    def wo_a(i):
+    # The step launches wo_a to overlap the kernel before it (the quantiser,
+    # which does not write the weights): the GEMM's prologue and weight reads
+    # run under it.  Timed alone, wo_a is measured both ways: back to back with
+    # the same overlap (the previous call writes only its own z) and serialised.
+    def wo_a(i, overlap=True):
         st = sets[i % nsets]
         if bf16:
             k.dsv4_grouped_wo_a_bf16(st["x"].transpose(0, 1), st["wo_a"], w.n_groups,
@@ -743,7 +789,10 @@ def run_workload(name: str, steps: int, warmup: int, local: int) -> dict:
             return
         k.dsv4_grouped_wo_a(st["x"].transpose(0, 1), st["xs"].permute(2, 0, 1)[:w.T],
                             st["wo_a"], st["wo_a_scale"], w.n_groups, w.o_lora_rank, z=st["z"],
-                            stream=stream)
+                            overlap_previous=overlap, stream=stream)
+
+    def wo_a_serial(i):
+        wo_a(i, overlap=False)
 
     # decode sizes: the quantiser fused into wo_a is timed beside the step (the
     # step is the two separate launches, the faster of the two at these sizes)
@@ -769,6 +818,7 @@ def run_workload(name: str, steps: int, warmup: int, local: int) -> dict:
         t_step = _graph_ms(step, steps, stream)
         t_q = _graph_ms(quant, steps, stream)
         t_a = _graph_ms(wo_a, steps, stream) if gemm else None
+        t_as = _graph_ms(wo_a_serial, steps, stream) if gemm and not bf16 else None
         t_f = _graph_ms(wo_a_fused, steps, stream) if fused else None
     ms_step, ms_q = t_step["ms"], t_q["ms"]
     ms_a = t_a["ms"] if gemm else 0.0
@@ -794,6 +844,13 @@ def run_workload(name: str, steps: int, warmup: int, local: int) -> dict:
             stages["wo_a"] = {"ms": ms_a, "bound": "tensor", "algorithmic": fl,
                               "achieved": fl / (ms_a * 1e-3) / 1e12, "unit": "TFLOP/s",
                               **spread(t_a)}
+    if t_as is not None:   # the same GEMM launched without overlap (not part of the step)
+        bound = stages["wo_a"]["bound"]
+        work = by if bound == "hbm" else fl
+        scale = 1e9 if bound == "hbm" else 1e12
+        stages["wo_a_serial"] = {"ms": t_as["ms"], "bound": bound, "algorithmic": work,
+                                 "achieved": work / (t_as["ms"] * 1e-3) / scale,
+                                 "unit": stages["wo_a"]["unit"], **spread(t_as)}
     if fused:   # one kernel: o and the weights in, z out (not part of the step)
         fb = w.T * w.H * 1024 + w.T * (8 + 256) + w.n_groups * w.o_lora_rank * w.D + \
             w.T * w.n_groups * w.o_lora_rank * 2
@@ -801,9 +858,11 @@ def run_workload(name: str, steps: int, warmup: int, local: int) -> dict:
                                       "achieved": fb / (t_f["ms"] * 1e-3) / 1e9, "unit": "GB/s",
                                       **spread(t_f)}
     for n_, s_ in stages.items():
-        region_s = {"quant": t_q, "wo_a": t_a, "fused_quant_wo_a": t_f}[n_]["ms"] * steps / 1e3
+        region_s = {"quant": t_q, "wo_a": t_a, "wo_a_serial": t_as,
+                    "fused_quant_wo_a": t_f}[n_]["ms"] * steps / 1e3
         add_roofline(s_, peaks, src, region_s, clocks, num_sms, dtype)
-    dom = max((n for n in stages if n != "fused_quant_wo_a"), key=lambda n: stages[n]["ms"])
+    dom = max((n for n in stages if n not in ("fused_quant_wo_a", "wo_a_serial")),
+              key=lambda n: stages[n]["ms"])
     ds = stages[dom]
     roofline = {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
                 "peak": ds["peak"], "unit": ds["unit"], "frac": ds["frac"],
@@ -818,6 +877,9 @@ def run_workload(name: str, steps: int, warmup: int, local: int) -> dict:
         "data": "synthetic (seeded; " + ("bf16 weights" if bf16 else
                                          "FP8 block-scaled weights drawn in stored form") +
                 ("; o drawn on the device" if on_device else "") + ")",
+        "launch": "wo_a launched to overlap the kernel before it (its prologue and weight "
+                  "reads under that kernel; wo_a_serial: the same GEMM without overlap)"
+                  if gemm and not bf16 else None,
         "config": {"workload": f"{name}: T={w.T}, {w.H} heads x 512 ({w.n_groups} "
                                f"groups x {w.heads_per_group})" +
                                (f", o_lora_rank {w.o_lora_rank}, " + ("bf16 inverse RoPE + bf16 "

@@ -54,6 +54,8 @@ def load_library() -> ctypes.CDLL:
     lib.dsv4_inv_rope_fp8_quant.argtypes = [P, P, P, I64, I64, I, I, I, I, I, P, P, P]
     lib.dsv4_inv_rope_fp8_quant.restype = I
     lib.dsv4_grouped_wo_a.argtypes = [P, P, I64, I, I, I, P, P, P, P]
+    lib.dsv4_grouped_wo_a_ex.argtypes = [P, P, I64, I, I, I, P, P, P, ctypes.c_uint, P]
+    lib.dsv4_grouped_wo_a_ex.restype = I
     lib.dsv4_inv_rope_grouped_wo_a.argtypes = [P, P, P, I64, I64, I, I, I, I, I, I, P, P, P, P]
     lib.dsv4_inv_rope_grouped_wo_a.restype = I
     lib.dsv4_grouped_wo_a.restype = I
@@ -169,11 +171,18 @@ def dsv4_inv_rope_fp8_quant(o: torch.Tensor, positions: torch.Tensor, cos_sin_ca
     return out_fp8.transpose(0, 1), out_scale.permute(2, 0, 1)[:T]
 
 
+OVERLAP_PREVIOUS = 1   # DSV4_OVERLAP_PREVIOUS
+
+
 def dsv4_grouped_wo_a(x_fp8: torch.Tensor, x_scale: torch.Tensor, w_fp8: torch.Tensor,
                       w_scale: torch.Tensor, n_groups: int, o_lora_rank: int, *,
-                      z: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                      z: torch.Tensor | None = None, overlap_previous: bool = False,
+                      stream=None) -> torch.Tensor:
     """x_fp8: the [T, G, D] view (strides (D, T*D, 1)) the quantiser returns;
-    x_scale: the matching [T, G, PK] view.  Returns bf16 z [T, G, R]."""
+    x_scale: the matching [T, G, PK] view.  Returns bf16 z [T, G, R].
+    overlap_previous: launch so that the kernel starts under the previous
+    kernel of the stream, reading only the weights until that one completes
+    (the caller guarantees that it does not write them)."""
     lib = load_library()
     _cuda(x_fp8, "x_fp8", _FP8)
     _cuda(x_scale, "x_scale", torch.int32)
@@ -192,8 +201,9 @@ def dsv4_grouped_wo_a(x_fp8: torch.Tensor, x_scale: torch.Tensor, w_fp8: torch.T
         raise ValueError("w_scale must be a contiguous [G*R/128, D/128] tensor")
     if z is None:
         z = torch.empty((T, G, o_lora_rank), dtype=torch.bfloat16, device=x_fp8.device)
-    rc = lib.dsv4_grouped_wo_a(x_fp8.data_ptr(), x_scale.data_ptr(), T, G, D, o_lora_rank,
-                               w_fp8.data_ptr(), w_scale.data_ptr(), z.data_ptr(), _stream(stream))
+    rc = lib.dsv4_grouped_wo_a_ex(x_fp8.data_ptr(), x_scale.data_ptr(), T, G, D, o_lora_rank,
+                                  w_fp8.data_ptr(), w_scale.data_ptr(), z.data_ptr(),
+                                  OVERLAP_PREVIOUS if overlap_previous else 0, _stream(stream))
     _check(rc, "dsv4_grouped_wo_a")
     return z
 

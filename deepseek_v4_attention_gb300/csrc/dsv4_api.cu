@@ -157,7 +157,15 @@ int dsv4_inv_rope_fp8_quant(const void* o, const int64_t* positions, const float
 int dsv4_grouped_wo_a(const void* x_fp8, const int32_t* x_scale, int64_t num_tokens,
                       int n_groups, int group_dim, int o_lora_rank, const void* w_fp8,
                       const uint8_t* w_scale, void* z, void* stream) {
+  return dsv4_grouped_wo_a_ex(x_fp8, x_scale, num_tokens, n_groups, group_dim, o_lora_rank, w_fp8,
+                              w_scale, z, 0u, stream);
+}
+
+int dsv4_grouped_wo_a_ex(const void* x_fp8, const int32_t* x_scale, int64_t num_tokens,
+                         int n_groups, int group_dim, int o_lora_rank, const void* w_fp8,
+                         const uint8_t* w_scale, void* z, unsigned flags, void* stream) {
   t_last_launches = 0;
+  if ((flags & ~DSV4_OVERLAP_PREVIOUS) != 0) return DSV4_ERR_SHAPE;
   if (num_tokens < 0 || n_groups <= 0 || group_dim <= 0 || o_lora_rank <= 0 ||
       group_dim % 128 != 0 || o_lora_rank % 128 != 0)
     return DSV4_ERR_SHAPE;
@@ -180,6 +188,7 @@ int dsv4_grouped_wo_a(const void* x_fp8, const int32_t* x_scale, int64_t num_tok
   p.b_scale = w_scale;
   p.epilogue = kEpiBf16;
   p.out_bf16 = z;
+  p.after_own_kernel = (flags & DSV4_OVERLAP_PREVIOUS) != 0;
   rc = launch_block_scaled_gemm(p, static_cast<cudaStream_t>(stream), dev);
   if (rc == DSV4_OK) t_last_launches = 1;
   return rc;

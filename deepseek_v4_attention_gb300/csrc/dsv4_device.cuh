@@ -164,6 +164,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Prefetch of a 2D box of a tensor into L2 (no shared memory, no completion
+// to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // TMA store of a 2D box from this CTA's shared memory, tracked as a bulk group.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x,
                                              int32_t y) {

@@ -135,6 +135,8 @@ struct Params {
   int64_t max_pos;
   int H, hpg;
   int raster_m;            // > 0: tiles in groups of raster_m m-blocks (G = 1), see tile_coords
+  int prefetch_l2;         // launched to overlap the previous kernel: before waiting for it,
+                           // prefetch the first tile's remaining weight k-blocks into L2
 };
 
 // Tile order.  Default: m-blocks fastest, then column tiles, then groups (the
@@ -209,6 +211,7 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
                              const __grid_constant__ CUtensorMap tm_out, const Params p) {
   using C = Cfg<kBN, kARows, kFused>;
   static_assert(!kFused || (!kBf16 && kARows == 64 && kBN == 128), "fused A: decode tiles");
+  static_assert(kSplit <= 2, "the split-K reduction has one partial buffer per warp slice");
   constexpr uint32_t kABytes = C::kABytes;
   constexpr int kStages = C::kStages;
   constexpr int kAccBufs = C::kAccBufs;
@@ -293,6 +296,12 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
           tma_load_2d(smem + C::b + i * kBBytes, &tm_b, &full[i],
                       (kb_begin<kSplit>(p) + i) * kBKe, brow);
         }
+        // The rest of the first tile's weights go to L2 while the previous
+        // kernel still runs, so that the weight-bound small-T shapes stream
+        // them from L2 once their activations are ready.
+        if (p.prefetch_l2)
+          for (int kb = kb_begin<kSplit>(p) + early; kb < kb_end<kSplit>(p); ++kb)
+            tma_prefetch_l2_2d(&tm_b, kb * kBKe, brow);
       }
       griddep_wait();
       for (int tile = first_tile<kSplit>(); tile < p.num_tiles && ok;
@@ -647,7 +656,10 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
         // (32 rows x 128 fp32) has its own 16 KiB there, laid out [col/4][lane].
         cluster_sync();
         const uint32_t part = smem_addr(smem + C::a) + static_cast<uint32_t>(epi) * 16384u;
-        if (split_rank<kSplit>() != 0) {
+        // a warp whose 32 rows all lie past the last token has nothing to add
+        // (those rows are never stored): it only meets the two barriers
+        const bool rows_live = static_cast<int64_t>(m_blk) * kBM + quarter * 32 < p.T;
+        if (split_rank<kSplit>() != 0 && rows_live) {
           const uint32_t dst = map_to_cta(part, 0);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -658,7 +670,7 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
         }
         cluster_sync();
         synced = true;
-        if (split_rank<kSplit>() == 0) {
+        if (split_rank<kSplit>() == 0 && rows_live) {
           for (int peer = 1; peer < kSplit; ++peer) {
             const float4* src = reinterpret_cast<const float4*>(smem + C::a + epi * 16384);
 #pragma unroll
@@ -826,9 +838,9 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
 
 template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows, bool kFused = false>
 int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
-  // q.after_own_kernel: the previous kernel on the stream is one of this
-  // library's (inside dsv4_o_proj), so the launch may overlap it: this kernel
-  // reads only weights before griddep_wait().
+  // q.after_own_kernel: the previous kernel on the stream does not write the
+  // weights (inside dsv4_o_proj it is one of this library's), so the launch
+  // may overlap it: this kernel reads only weights before griddep_wait().
   using C = Cfg<kBN, kARows, kFused>;
   static std::atomic<int> configured_for[kMaxDevices];
   if (dev.device < 0 || dev.device >= kMaxDevices) return DSV4_ERR_UNSUPPORTED;
@@ -918,6 +930,7 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   p.H = q.heads;
   p.hpg = q.heads_per_group;
   p.raster_m = (q.G == 1 && p.m_tiles > kRasterM) ? kRasterM : 0;
+  p.prefetch_l2 = q.after_own_kernel ? 1 : 0;
 
   // persistent: one CTA per SM; split-K: one cluster of kSplit CTAs per tile
   const int grid = kSplit == 1 ? (p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms)

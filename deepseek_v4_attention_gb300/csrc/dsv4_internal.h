@@ -63,8 +63,9 @@ struct GemmProblem {
   const uint8_t* b_scale = nullptr; // UE8M0 bytes [G*N/128][K/128]
   int epilogue = kEpiBf16;
   bool bf16 = false;                // A and B bf16, no scales (kind::f16), K % 64 == 0
-  bool after_own_kernel = false;    // previous kernel on the stream is this library's own:
-                                    // launch with programmatic stream serialization
+  bool after_own_kernel = false;    // the previous kernel on the stream does not write the
+                                    // weights (b, b_scale): launch with programmatic stream
+                                    // serialization and read them before it completes
   // Fused A (decode sizes, T <= 64): the kernel's producer warps build A from
   // the attention output (inverse rotation + per-128 FP8 quantisation, the
   // quantiser's arithmetic) instead of reading a pre-quantised a / a_scale;

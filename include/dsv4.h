@@ -111,6 +111,29 @@ int dsv4_grouped_wo_a(const void* x_fp8, const int32_t* x_scale, int64_t num_tok
                       int n_groups, int group_dim, int o_lora_rank, const void* w_fp8,
                       const uint8_t* w_scale, void* z, void* stream);
 
+/* Launch option of dsv4_grouped_wo_a_ex. */
+#define DSV4_OVERLAP_PREVIOUS 1u
+
+/*
+ * dsv4_grouped_wo_a with launch options (flags = 0: exactly dsv4_grouped_wo_a).
+ *
+ * DSV4_OVERLAP_PREVIOUS: the kernel is launched with programmatic stream
+ * serialization, so that it starts while the previous kernel on `stream`
+ * still runs: its prologue and its reads of w_fp8 and w_scale (the first
+ * pipeline stages into shared memory, the rest of each CTA's first weight
+ * tile into L2) overlap that kernel, and every read of x_fp8 / x_scale and
+ * every write of z waits until that kernel has completed.  For the
+ * weight-read-bound decode shapes this hides the launch and much of the
+ * weight stream behind the kernel before (in a decode step, the quantiser).
+ * The caller guarantees that the previous kernel on the stream does not write
+ * w_fp8 or w_scale (weights loaded once and then only read).
+ *
+ * Errors: as dsv4_grouped_wo_a; DSV4_ERR_SHAPE for an unknown flag bit.
+ */
+int dsv4_grouped_wo_a_ex(const void* x_fp8, const int32_t* x_scale, int64_t num_tokens,
+                         int n_groups, int group_dim, int o_lora_rank, const void* w_fp8,
+                         const uint8_t* w_scale, void* z, unsigned flags, void* stream);
+
 /* Largest token count the fused path below serves (decode sizes). */
 #define DSV4_FUSED_MAX_TOKENS 64
 

@@ -23,6 +23,7 @@ def test_exports_every_header_function(lib):
                           "dsv4_o_proj_static", "dsv4_selftest_wait_timeout",
                           "dsv4_inv_rope_bf16", "dsv4_grouped_wo_a_bf16",
                           "dsv4_inv_rope_grouped_wo_a", "dsv4_static_scratch_bytes",
+                          "dsv4_grouped_wo_a_ex",
                           "dsv4_o_proj_partial", "dsv4_sum_partials",
                           "dsv4_rope_quant_unsupported_reason",
                           "dsv4_o_proj_prequant_workspace_bytes", "dsv4_o_proj_prequant",

@@ -358,3 +358,38 @@ def test_fused_wo_a_out_of_range_position(dev):
     zf, zs, sf, ss = _fused_and_separate(w, d, dev)
     assert k.STATUS[sf] == "DSV4_ERR_RANGE" and ss == sf
     assert np.array_equal(zf, zs)
+
+
+@pytest.mark.parametrize("name,T", [("decode", 64), ("decode", 7), ("prefill", 300)])
+def test_grouped_wo_a_overlapping_the_quantiser(dev, name, T):
+    """wo_a launched to overlap the kernel before it (DSV4_OVERLAP_PREVIOUS):
+    the quantiser overwrites x with another token batch just before, on the
+    same stream, and z must be that of the new x, bit-identical to the
+    serialised launch (x is read only after the quantiser has completed)."""
+    import deepseek_v4_attention_gb300 as k
+    w = di.WORKLOADS[name].with_tokens(T, seed=T + 21)
+    d1 = di.make_inputs(w, with_wo_b=False)
+    d2 = di.make_inputs(w.with_tokens(T, seed=T + 22), with_wo_b=False)
+    wa, was = d1["wo_a"].to(dev), d1["wo_a_scale"].to(dev)
+    cache = d1["cache"].to(dev)
+    x = torch.empty(w.n_groups, T, w.D, dtype=torch.float8_e4m3fn, device=dev)
+    xs = torch.empty(w.n_groups, (w.D // 128 + 3) // 4, k.tma_aligned_tokens(T),
+                     dtype=torch.int32, device=dev)
+
+    def quant(d):
+        return k.dsv4_inv_rope_fp8_quant(d["o"].to(dev), d["positions"].to(dev), cache,
+                                         w.n_groups, w.heads_per_group, out_fp8=x, out_scale=xs)
+
+    quant(d1)
+    torch.cuda.synchronize()
+    q, s = quant(d2)
+    z_ov = k.dsv4_grouped_wo_a(q, s, wa, was, w.n_groups, w.o_lora_rank, overlap_previous=True)
+    torch.cuda.synchronize()
+    z_se = k.dsv4_grouped_wo_a(q, s, wa, was, w.n_groups, w.o_lora_rank)
+    torch.cuda.synchronize()
+    assert k.dsv4_device_status(clear=True) == 0
+    assert torch.equal(z_ov.view(torch.int16), z_se.view(torch.int16))
+    lib = k.load_library()
+    assert lib.dsv4_grouped_wo_a_ex(q.data_ptr(), s.data_ptr(), T, w.n_groups, w.D,
+                                    w.o_lora_rank, wa.data_ptr(), was.data_ptr(),
+                                    z_se.data_ptr(), 2, None) == -1      # unknown flag bit
