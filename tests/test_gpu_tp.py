@@ -204,3 +204,10 @@ def test_o_proj_prequant_errors(dev):
     torch.cuda.synchronize()
     assert k.dsv4_device_status(clear=True) == 0
     assert bool((out == 0).all())                        # zero codes: zero output
+
+
+@pytest.mark.parametrize("T", [1024, 777])
+def test_single_share_equals_the_layer_large(dev, T):
+    """The fp32 share at sizes where both GEMMs take the 256-wide persistent
+    tiles, rounded by dsv4_sum_partials: bit-identical to dsv4_o_proj."""
+    test_single_share_equals_the_layer(dev, "full", T)
