@@ -478,7 +478,8 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
       if constexpr (!kFused) load_pack(kb0 / 4, vnext);   // fused A: the producers write SFA
       uint32_t bword[kRb];
       for (int kb = kb0; kb < kb_end<kSplit>(p); ++kb) {
-        if (kb == kb0 || (kb & 3) == 0) {   // a new pack: its words, and the next pack's load
+        const bool pack_start = kb == kb0 || (kb & 3) == 0;
+        if (pack_start) {   // a new pack: its words, and the next pack's load
           const int j = kb / 4;
           if constexpr (!kFused) {
 #pragma unroll
@@ -497,12 +498,18 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
             ? mbar_wait_warp_lazy(&empty[stage], phase ^ 1u, abort_flag, p.status, 64)
             : mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.status);
         if (!got) { ok = false; break; }
-        uint4* dst = reinterpret_cast<uint4*>(smem + C::sf + stage * C::kSfSlotBytes);
-        if constexpr (!kFused) dst[lane] = make_uint4(vcur[0], vcur[1], vcur[2], vcur[3]);
+        // The MMA thread copies a slot to TMEM only at the first k-block of a
+        // pack (fused A: every k-block, whose A scale byte the producers write),
+        // so only those slots are written; for the others this warp only
+        // arrives once the stage is free.
+        if (kFused || pack_start) {
+          uint4* dst = reinterpret_cast<uint4*>(smem + C::sf + stage * C::kSfSlotBytes);
+          if constexpr (!kFused) dst[lane] = make_uint4(vcur[0], vcur[1], vcur[2], vcur[3]);
 #pragma unroll
-        for (int r = 0; r < kRb; ++r)
-          dst[32 + 32 * r + lane] = make_uint4(bword[r], bword[r], bword[r], bword[r]);
-        fence_proxy_async_smem();
+          for (int r = 0; r < kRb; ++r)
+            dst[32 + 32 * r + lane] = make_uint4(bword[r], bword[r], bword[r], bword[r]);
+          fence_proxy_async_smem();
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[stage]);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
