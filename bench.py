@@ -275,7 +275,7 @@ def summarize_traffic(csv_path: str) -> str:
     for src in TRAFFIC_SOURCES:
         with open(os.path.join(csrc, src), "rb") as g:
             lines.append(f"source {src} {hashlib.sha256(g.read()).hexdigest()}")
-    lines.append("# kernel  read_bytes  write_bytes  duration_us (ten launches each)")
+    lines.append("# kernel  read_bytes  write_bytes  duration_us (one line per captured launch)")
     for k in ("quant", "wo_a", "wo_b"):
         for name, m in launches.values():
             if kernel_of(name) == k:

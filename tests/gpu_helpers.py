@@ -73,6 +73,8 @@ def rel_errs(gpu_bf16_bits: np.ndarray, ref64: np.ndarray) -> tuple[np.ndarray, 
     g = bf16_bits_to_f64(gpu_bf16_bits)
     ref = ref64.astype(np.float64).reshape(g.shape)
     rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 1.0
+    if rms == 0.0:
+        rms = 1.0        # an identically zero reference: the absolute error
     return np.abs(g - ref), np.maximum(np.abs(ref), rms)
 
 

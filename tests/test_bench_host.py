@@ -73,3 +73,40 @@ def test_recorded_traffic_reads_the_committed_record_format(tmp_path, monkeypatc
     assert bench.recorded_traffic("wo_a") is None          # no lines for it
     (csrc / bench.TRAFFIC_SOURCES[0]).write_bytes(b"// changed\n")
     assert bench.recorded_traffic("wo_b") is None
+
+
+def test_tensor_peak_rule():
+    """Burst cuBLAS bf16 figure for sub-second timed regions, the sustained one
+    from a second on; FP8 = 2 x bf16."""
+    peaks = {"hbm_gbs": 6663.2, "bf16_tflops": 1902.6, "bf16_tflops_sustained": 1719.6}
+    p, rule = bench.tensor_peak(peaks, "measured", 0.013, "e4m3")
+    assert p == 2 * 1902.6 and "burst" in rule and "13.0 ms" in rule
+    p, rule = bench.tensor_peak(peaks, "measured", 2.5, "e4m3")
+    assert p == 2 * 1719.6 and "sustained" in rule
+    p, _ = bench.tensor_peak(peaks, "measured", 0.5, "bf16")
+    assert p == 1902.6
+    p, _ = bench.tensor_peak({"hbm_gbs": 1.0, "bf16_tflops": 100.0}, "fallback", 5.0, "e4m3")
+    assert p == 200.0                                  # no sustained figure: burst
+
+
+def test_add_roofline_clock_matched():
+    peaks = {"hbm_gbs": 6663.2, "bf16_tflops": 1902.6, "bf16_tflops_sustained": 1719.6}
+    st = {"ms": 0.3, "bound": "tensor", "achieved": 3000.0, "unit": "TFLOP/s"}
+    bench.add_roofline(st, peaks, "measured", 0.013, {"sm_mhz": 2000.0}, 152)
+    cm = 16384 * 152 * 2000e6 / 1e12
+    assert abs(st["clock_matched"]["peak"] - cm) < 1e-9
+    assert abs(st["clock_matched"]["frac"] - 3000.0 / cm) < 1e-12
+    assert abs(st["tflops_per_ghz"] - 1500.0) < 1e-9
+    assert abs(st["frac"] - 3000.0 / (2 * 1902.6)) < 1e-12
+    hb = {"ms": 0.1, "bound": "hbm", "achieved": 6000.0, "unit": "GB/s"}
+    bench.add_roofline(hb, peaks, "measured", 0.013, {"sm_mhz": None}, 152)
+    assert hb["peak"] == 6663.2 and "clock_matched" not in hb
+
+
+def test_clock_sampler_summary():
+    s = bench.ClockSampler(0)
+    s.samples = [(2070.0, 900.0, []), (1950.0, 1400.0, ["sw_power_cap"]), (2010.0, None, [])]
+    s.max_mhz = 2070.0
+    out = s.summary()
+    assert out["sm_mhz"] == 2010.0 and out["samples"] == 3 and out["sm_mhz_min"] == 1950.0
+    assert out["reasons"] == ["sw_power_cap"] and out["power_w_max"] == 1400.0

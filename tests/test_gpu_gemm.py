@@ -393,3 +393,54 @@ def test_grouped_wo_a_overlapping_the_quantiser(dev, name, T):
     assert lib.dsv4_grouped_wo_a_ex(q.data_ptr(), s.data_ptr(), T, w.n_groups, w.D,
                                     w.o_lora_rank, wa.data_ptr(), was.data_ptr(),
                                     z_se.data_ptr(), 2, None) == -1      # unknown flag bit
+
+
+def test_o_proj_all_zero_input(dev):
+    """The degenerate input: o all zero.  Every 128-block of x and of zq has the
+    floor scale (amax floored at 1e-4: byte 105), every code is +-0, and the
+    output is exactly zero."""
+    import deepseek_v4_attention_gb300 as k
+    w = di.WORKLOADS["full"].with_tokens(37, seed=3)
+    d = di.make_inputs(w)
+    d["o"] = torch.zeros_like(d["o"])
+    out, ws = _o_proj_gpu(d, w, dev)
+    parts = k.o_proj_workspace_views(ws, w.T, w.n_groups, w.heads_per_group, w.head_dim,
+                                     w.o_lora_rank)
+    assert bool((out.view(torch.int16) == 0).all())
+    for name in ("x", "zq"):
+        c = parts[name].cpu()
+        assert bool(((c & 0x7F) == 0).all()), name
+    xs = parts["xs"].cpu().numpy()[:, :, :w.T].view(np.uint8)
+    assert (xs == 105).all()
+    zs = parts["zs"].cpu().numpy()[:, :w.T].view(np.uint8)
+    assert (zs == 105).all()            # G*R/128 = 128 blocks: every byte is a block
+    check_o_proj_parts(d, w, out, ws)
+
+
+@pytest.mark.parametrize("D", [65536])
+def test_grouped_wo_a_largest_k(dev, D):
+    """K = 65536, the largest reduction whose weight-scale words (128 packs of
+    four 128-blocks) the GEMM holds per lane: every branch of the pack lookup."""
+    T, G, R = 5, 1, 128
+    T_al = oracle.tma_aligned_tokens(T)
+    x, xs = di.random_fp8_activation(T, G, D, seed=91, tma_aligned_T=T_al)
+    w, ws = di.fp8_block_weight(G * R, D, seed=92)
+    zg = _gpu_wo_a(x, xs, w, ws, T, G, D, R, dev)
+    _, z64 = oracle.grouped_gemm(x, xs, w, ws, T, G, D, R, want_fp64=True)
+    assert gemm_rel_err(zg, z64) <= GEMM_RTOL
+
+
+def test_grouped_wo_a_k_beyond_the_limit_is_rejected(dev):
+    import deepseek_v4_attention_gb300 as k
+    lib = k.load_library()
+    T, D, R = 4, 65536 + 128, 128
+    x = torch.zeros(T, D, dtype=torch.uint8, device=dev)
+    xs = torch.zeros((D // 128 + 3) // 4, T, dtype=torch.int32, device=dev)
+    w = torch.zeros(R, D, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(1, D // 128, dtype=torch.uint8, device=dev)
+    z = torch.full((T, R), 7, dtype=torch.int16, device=dev)
+    rc = lib.dsv4_grouped_wo_a(x.data_ptr(), xs.data_ptr(), T, 1, D, R, w.data_ptr(),
+                               ws.data_ptr(), z.data_ptr(), None)
+    assert rc == k._NAME_TO_CODE["DSV4_ERR_UNSUPPORTED"]
+    torch.cuda.synchronize()
+    assert bool((z == 7).all())          # nothing was launched
