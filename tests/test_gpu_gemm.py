@@ -328,10 +328,10 @@ def _fused_and_separate(w, d, dev):
 
 
 # (T, G, hpg, R): split-K cluster tiles (even hpg, few tiles), one CTA per tile
-# (hpg = 1, or 128 tiles), ragged T, a single token
+# (hpg = 1, or 128 tiles), ragged T, a single token, column-tile counts 1-16
 @pytest.mark.parametrize("T,G,hpg,R", [(1, 2, 2, 128), (7, 8, 8, 1024), (16, 2, 2, 128),
                                        (33, 4, 4, 256), (64, 8, 8, 1024), (64, 16, 8, 1024),
-                                       (5, 3, 1, 384)])
+                                       (5, 3, 1, 384), (12, 2, 2, 512), (64, 1, 8, 2048)])
 def test_fused_wo_a_equals_quant_then_gemm(dev, T, G, hpg, R):
     """The fused producer runs the quantiser's arithmetic: z is bit-identical to
     dsv4_grouped_wo_a of dsv4_inv_rope_fp8_quant's output, and within the GEMM
