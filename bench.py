@@ -686,7 +686,7 @@ def run_reference(args, ws, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded; random FP8 block-scaled weights)",
+        "data": "synthetic (seeded; FP8 block-scaled weights drawn in stored form)",
         "config": config_of(w, ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{n} tokens per step of the workload's {w.T}"},

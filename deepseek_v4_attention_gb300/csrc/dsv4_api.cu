@@ -93,7 +93,7 @@ int get_device_info(DeviceInfo* out) {
               cudaSuccess)
         return DSV4_ERR_CUDA;
       d.max_smem_optin = static_cast<size_t>(v);
-      // this build carries sm_103a code only
+      // the library carries sm_103a code only
       if (d.cc_major != 10 || d.cc_minor != 3) return DSV4_ERR_UNSUPPORTED;
       void* sym = nullptr;
       if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess || sym == nullptr)

@@ -40,7 +40,7 @@ typedef enum dsv4_status {
     DSV4_ERR_SHAPE = -1,       /* a shape assert of fused_inv_rope_fp8_quant, or a size rule below */
     DSV4_ERR_NULL = -2,        /* a required pointer is NULL                                      */
     DSV4_ERR_ALIGN = -3,       /* a base pointer is not 16-byte aligned (TMA and vector loads)    */
-    DSV4_ERR_UNSUPPORTED = -4, /* not an sm_103 device, or a parameter this build does not serve  */
+    DSV4_ERR_UNSUPPORTED = -4, /* not an sm_103 device, or a parameter the library does not serve */
     DSV4_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than dsv4_o_proj_workspace_bytes()    */
     DSV4_ERR_CUDA = -6,        /* a CUDA runtime/driver call failed (launch error included)       */
     DSV4_ERR_TIMEOUT = -7,     /* device status: a kernel pipeline wait ran out of time           */

@@ -123,7 +123,7 @@ def test_quant_empty_and_errors(dev):
     assert lib.dsv4_inv_rope_fp8_quant(*bad) == -1
     bad = list(args); bad[9] = 32                        # nope % qgs != qgs - rope
     assert lib.dsv4_inv_rope_fp8_quant(*bad) == -1
-    bad = list(args); bad[7], bad[8] = 192, 64           # valid asserts, not this build's head
+    bad = list(args); bad[7], bad[8] = 192, 64           # valid asserts, a head the library does not serve
     assert lib.dsv4_inv_rope_fp8_quant(*bad) == -4
     bad = list(args); bad[4] = 0                         # max_pos
     assert lib.dsv4_inv_rope_fp8_quant(*bad) == -1
