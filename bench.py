@@ -242,7 +242,8 @@ def recorded_traffic(kernel: str) -> float | None:
     return sum(vals) / len(vals) if vals else None
 
 
-TRAFFIC_SOURCES = ("dsv4_gemm.cu", "dsv4_quant.cu", "dsv4_device.cuh")
+TRAFFIC_SOURCES = ("dsv4_gemm.cu", "dsv4_gemm_pair.cu", "dsv4_gemm_common.cuh", "dsv4_quant.cu",
+                   "dsv4_device.cuh")
 
 
 def summarize_traffic(csv_path: str) -> str:
@@ -268,7 +269,9 @@ def summarize_traffic(csv_path: str) -> str:
     def kernel_of(name: str) -> str:
         if "inv_rope" in name:
             return "quant"
-        return "wo_a" if "<256, 1," in name else "wo_b"   # the re-quantising epilogue
+        # the re-quantising epilogue (kEpi = 1) is wo_a's: the first template
+        # argument of the CTA-pair kernel, the second of the one-SM kernel
+        return "wo_a" if ("pair_kernel<1>" in name or "<256, 1," in name) else "wo_b"
 
     csrc = os.path.join(ROOT, "deepseek_v4_attention_gb300", "csrc")
     lines = []

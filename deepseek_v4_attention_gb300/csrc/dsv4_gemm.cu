@@ -49,21 +49,11 @@
 // scaled by the same power of two.  The byte is chosen with the
 // scale-factor-id field of the instruction descriptor: the 4 blocks of a
 // packed int32 are bytes 0..3 of one TMEM column word.
-#include <string.h>
-
-#include "dsv4_device.cuh"
-#include "dsv4_internal.h"
+#include "dsv4_gemm_common.cuh"
 
 namespace dsv4 {
 
 namespace {
-
-constexpr int kBM = 128;
-constexpr int kBK = 128;
-constexpr int kTmemCols = 512;
-constexpr int kRasterM = 16;   // m-blocks per raster group (G = 1); 8 measured worse
-
-constexpr uint32_t kSfaBytes = kBM * 4;    // 512 B
 
 // Tile configuration.  kBN = 128: two 128-column TMEM accumulators (the
 // epilogue of tile i overlaps the MMAs of tile i+1), 4 epilogue warps.
@@ -76,10 +66,21 @@ constexpr uint32_t kSfaBytes = kBM * 4;    // 512 B
 // 64 rows (the next bytes of shared memory) only reach accumulator rows that
 // are never stored.  The smaller stage fits 8 stages instead of 6, a third more
 // weight bytes in flight per CTA.
-template <int kBN, int kARows = 128, bool kFused = false>
+//
+// kKps = 2: a pipeline stage holds two consecutive k-blocks (eight MMAs) behind
+// one full and one empty barrier, so the MMA thread waits and commits once
+// per eight MMAs instead of once per four.  The tensor pipe only stays busy if
+// the issuing thread queues MMAs faster than it drains them; a barrier wait
+// between groups of four MMAs measured ~0.7-0.8 of the ideal issue rate even
+// with operands resident, a wait per eight 1.0.  The shared memory holds the
+// same k-blocks (kSlots), in half as many stages.
+template <int kBN, int kARows = 128, bool kFused = false, int kKps = 1>
 struct Cfg {
+  static_assert(kKps == 1 || (kKps == 2 && !kFused), "two k-blocks per stage: unfused A only");
   static constexpr uint32_t kABytes = kARows * kBK;
-  static constexpr int kStages = kFused ? 6 : (kARows == 64) ? 8 : (kBN == 128) ? 6 : 4;
+  // k-block buffers (A and B tiles) and the stages that group them
+  static constexpr int kSlots = kFused ? 6 : (kARows == 64) ? 8 : (kBN == 128) ? 6 : 4;
+  static constexpr int kStages = kSlots / kKps;
   static constexpr int kAccBufs = (kBN == 128) ? 2 : 1;
   static constexpr int kEpiWarps = (kBN == 128) ? 4 : 8;
   static constexpr int kEpiWarp0 = 3;
@@ -89,7 +90,8 @@ struct Cfg {
   static constexpr int kProdWarp0 = kEpiWarp0 + kEpiWarps;
   static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + kProdWarps);
   static constexpr uint32_t kBBytes = kBN * kBK;
-  static constexpr int kSfSlots = kStages;   // one scale-factor slot per stage
+  static constexpr int kSfSlots = kStages;   // one scale-factor slot per stage (a stage
+                                             // holds at most one pack start, see the kernel)
   static constexpr uint32_t kSfbBytes = kBN * 4;
   static constexpr uint32_t kSfSlotBytes = kSfaBytes + kSfbBytes;
   static constexpr int kSfCol0 = kAccBufs * kBN;              // after the accumulators
@@ -97,8 +99,8 @@ struct Cfg {
   static_assert(kSfCol0 + kSfSlots * kSfColsPerSlot <= kTmemCols, "TMEM budget");
   // shared memory plan (operand tiles 1024-byte aligned for the 128B swizzle)
   static constexpr uint32_t a = 0;
-  static constexpr uint32_t b = a + kStages * kABytes;
-  static constexpr uint32_t sf = b + kStages * kBBytes;
+  static constexpr uint32_t b = a + kSlots * kABytes;
+  static constexpr uint32_t sf = b + kSlots * kBBytes;
   // fused A: a ring of kOStages bf16 slices of the attention output (kARows
   // token rows x 128 elements of one head, 256 B a row), loaded by TMA ahead
   // of the producer warps
@@ -115,67 +117,6 @@ struct Cfg {
   static constexpr uint32_t total = misc + 16;
   static constexpr uint32_t smem_bytes = total + 1024;  // + alignment slack
 };
-
-struct Params {
-  int64_t T;
-  int G, N, K;
-  int m_tiles, n_tiles, num_tiles, k_blocks, packs;
-  int64_t t_al;
-  const int32_t* a_scale;  // int32 [G][packs][t_al]
-  const uint8_t* b_scale;
-  int b_scale_ld;          // K / 128
-  __nv_bfloat16* out;      // [T][G*N] or null
-  uint8_t* q_out;          // [T][G*N]
-  int32_t* q_scale;        // [ceil(G*N/512)][t_al]
-  int* status;             // device status word
-  // fused A only
-  const uint16_t* o;       // bf16 [T][H][512]
-  const int64_t* positions;
-  const float* cache;      // fp32 [max_pos][64]
-  int64_t max_pos;
-  int H, hpg;
-  int raster_m;            // > 0: tiles in groups of raster_m m-blocks (G = 1), see tile_coords
-  int prefetch_l2;         // launched to overlap the previous kernel: before waiting for it,
-                           // prefetch the first tile's remaining weight k-blocks into L2
-};
-
-// Tile order.  Default: m-blocks fastest, then column tiles, then groups (the
-// column tiles of one group's m-block run in the same wave and share its A tile
-// in L2).  raster_m > 0 (a single group with many m-blocks, the dense wo_b):
-// groups of raster_m m-blocks, column tiles within a group, so that a wave
-// re-reads only its group's share of A (measured at T = 4096: DRAM reads of
-// wo_b 536 -> 411 MB).
-__device__ __forceinline__ void tile_coords(const Params& p, int tile, int& g, int& n_blk,
-                                            int& m_blk) {
-  if (p.raster_m > 0) {
-    const int per_group = p.raster_m * p.n_tiles;
-    const int grp = tile / per_group;
-    const int idx = tile - grp * per_group;
-    const int rest_m = p.m_tiles - grp * p.raster_m;
-    const int m_in = rest_m < p.raster_m ? rest_m : p.raster_m;   // the last group may be short
-    n_blk = idx / m_in;
-    m_blk = grp * p.raster_m + (idx - n_blk * m_in);
-    g = 0;
-    return;
-  }
-  m_blk = tile % p.m_tiles;
-  const int rest = tile / p.m_tiles;
-  n_blk = rest % p.n_tiles;
-  g = rest / p.n_tiles;
-}
-
-// Packed scale word of weight row block `rb` for k-blocks 4j..4j+3 (bytes
-// beyond the last k-block are 0).
-__device__ __forceinline__ uint32_t b_scale_word(const Params& p, int rb, int j) {
-  const uint8_t* row = p.b_scale + static_cast<int64_t>(rb) * p.b_scale_ld;
-  uint32_t w = 0;
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const int kb = 4 * j + b;
-    if (kb < p.k_blocks) w |= static_cast<uint32_t>(__ldg(row + kb)) << (8 * b);
-  }
-  return w;
-}
 
 // Tile schedule.  kSplit = 1: a persistent CTA walks tiles blockIdx.x,
 // blockIdx.x + gridDim.x, ... over all k-blocks.  kSplit > 1: a cluster of
@@ -204,12 +145,17 @@ __device__ __forceinline__ int kb_end(const Params& p) {
   return kSplit > 1 ? kb_begin<kSplit>(p) + p.k_blocks / kSplit : p.k_blocks;
 }
 
-template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows, bool kFused>
-__global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
+// Stages of kKps k-blocks: stage s holds the A and B tiles of its k-blocks in
+// buffers kKps s .. kKps s + kKps - 1.  A k-range starts at an even k-block
+// (0, or a multiple of four for the split-K halves), so a two-k-block stage
+// never straddles a pack of four: only a stage's first k-block can start a
+// pack.  The last stage of an odd k-range holds one k-block.
+template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows, bool kFused, int kKps>
+__global__ void __launch_bounds__(Cfg<kBN, kARows, kFused, kKps>::kThreads, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b,
                              const __grid_constant__ CUtensorMap tm_out, const Params p) {
-  using C = Cfg<kBN, kARows, kFused>;
+  using C = Cfg<kBN, kARows, kFused, kKps>;
   static_assert(!kFused || (!kBf16 && kARows == 64 && kBN == 128), "fused A: decode tiles");
   static_assert(kSplit <= 2, "the split-K reduction has one partial buffer per warp slice");
   constexpr uint32_t kABytes = C::kABytes;
@@ -283,24 +229,32 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
       // Before the previous kernel of the stream has finished (programmatic
       // launch) only the weights may be read: the first stages of the first
       // tile get their B tile now and their A tile after griddep_wait().
-      int early = 0;
+      // bytes that land on a stage's full barrier for n k-blocks (fused A:
+      // the producer warps write A; only B travels by TMA)
+      auto stage_tx = [](int n) {
+        return static_cast<uint32_t>(n) * (kFused ? kBBytes : kABytes + kBBytes);
+      };
+      int early = 0;   // stages
       if (first_tile<kSplit>() < p.num_tiles) {
         int g, n_blk, m_blk;
         tile_coords(p, first_tile<kSplit>(), g, n_blk, m_blk);
         const int brow = g * p.N + n_blk * kBN;
-        const int kbs = kb_end<kSplit>(p) - kb_begin<kSplit>(p);
-        early = kbs < kStages ? kbs : kStages;
+        const int kb0 = kb_begin<kSplit>(p), kb1 = kb_end<kSplit>(p);
+        const int nst = (kb1 - kb0 + kKps - 1) / kKps;
+        early = nst < kStages ? nst : kStages;
         for (int i = 0; i < early; ++i) {
-          // fused A: the producer warps write A; only B travels by TMA
-          mbar_arrive_expect_tx(&full[i], kFused ? kBBytes : kABytes + kBBytes);
-          tma_load_2d(smem + C::b + i * kBBytes, &tm_b, &full[i],
-                      (kb_begin<kSplit>(p) + i) * kBKe, brow);
+          const int kbs = kb0 + i * kKps;
+          const int n = (kKps == 1 || kb1 - kbs >= kKps) ? kKps : kb1 - kbs;
+          mbar_arrive_expect_tx(&full[i], stage_tx(n));
+          for (int j = 0; j < n; ++j)
+            tma_load_2d(smem + C::b + (i * kKps + j) * kBBytes, &tm_b, &full[i],
+                        (kbs + j) * kBKe, brow);
         }
         // The rest of the first tile's weights go to L2 while the previous
         // kernel still runs, so that the weight-bound small-T shapes stream
         // them from L2 once their activations are ready.
         if (p.prefetch_l2)
-          for (int kb = kb_begin<kSplit>(p) + early; kb < kb_end<kSplit>(p); ++kb)
+          for (int kb = kb0 + early * kKps; kb < kb1; ++kb)
             tma_prefetch_l2_2d(&tm_b, kb * kBKe, brow);
       }
       griddep_wait();
@@ -310,8 +264,11 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
         tile_coords(p, tile, g, n_blk, m_blk);
         [[maybe_unused]] const int m0 = m_blk * kBM;
         const int brow = g * p.N + n_blk * kBN;
-        for (int kb = kb_begin<kSplit>(p); kb < kb_end<kSplit>(p); ++kb) {
+        for (int kbs = kb_begin<kSplit>(p); kbs < kb_end<kSplit>(p); kbs += kKps) {
+          const int n = (kKps == 1 || kb_end<kSplit>(p) - kbs >= kKps) ? kKps
+                                                                       : kb_end<kSplit>(p) - kbs;
           if constexpr (kFused) {
+            const int kb = kbs;   // one k-block per stage
             // this k-block's slice of o: rows m0.., head g*hpg + kb/4, elements
             // (kb % 4)*128 .. +127 (rows past T zero-filled)
             if (!mbar_wait(&o_empty[oj], ophase ^ 1u, abort_flag, p.status)) { ok = false; break; }
@@ -324,7 +281,9 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
           }
           if (early > 0) {  // B already in flight for this stage
             if constexpr (!kFused)
-              tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBKe, m0, g);
+              for (int j = 0; j < n; ++j)
+                tma_load_3d(smem + C::a + (stage * kKps + j) * kABytes, &tm_a, &full[stage],
+                            (kbs + j) * kBKe, m0, g);
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -332,10 +291,14 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
             continue;
           }
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], kFused ? kBBytes : kABytes + kBBytes);
-          if constexpr (!kFused)
-            tma_load_3d(smem + C::a + stage * kABytes, &tm_a, &full[stage], kb * kBKe, m0, g);
-          tma_load_2d(smem + C::b + stage * kBBytes, &tm_b, &full[stage], kb * kBKe, brow);
+          mbar_arrive_expect_tx(&full[stage], stage_tx(n));
+          for (int j = 0; j < n; ++j) {
+            if constexpr (!kFused)
+              tma_load_3d(smem + C::a + (stage * kKps + j) * kABytes, &tm_a, &full[stage],
+                          (kbs + j) * kBKe, m0, g);
+            tma_load_2d(smem + C::b + (stage * kKps + j) * kBBytes, &tm_b, &full[stage],
+                        (kbs + j) * kBKe, brow);
+          }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -369,7 +332,7 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
       // the byte), so they are copied to TMEM once per pack, into region
       // (packs so far) mod kStages.  A region is rewritten kStages packs later,
       // by which time the full-barrier wait of that stage proves every MMA at
-      // least kStages k-blocks back complete, the old pack's included.  (The
+      // least kStages stages back complete, the old pack's included.  (The
       // fused A role writes one byte per stage; it copies every stage.)
       int sf_region = kStages - 1;
       for (int tile = first_tile<kSplit>(); tile < p.num_tiles && ok;
@@ -377,11 +340,14 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
         if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        for (int kb = kb_begin<kSplit>(p); kb < kb_end<kSplit>(p); ++kb) {
+        const int kb0 = kb_begin<kSplit>(p);
+        for (int kbs = kb0; kbs < kb_end<kSplit>(p); kbs += kKps) {
+          const int n = (kKps == 1 || kb_end<kSplit>(p) - kbs >= kKps) ? kKps
+                                                                       : kb_end<kSplit>(p) - kbs;
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           // the stage's scale factors arrived with its operands (same barrier)
-          const bool pack_start = kb == kb_begin<kSplit>(p) || (kb & 3) == 0;
+          const bool pack_start = kbs == kb0 || (kbs & 3) == 0;
           if (pack_start) sf_region = (sf_region + 1 == kStages) ? 0 : sf_region + 1;
           const uint32_t sf_col = tmem_base + static_cast<uint32_t>(
               C::kSfCol0 + (kFused ? stage : sf_region) * C::kSfColsPerSlot);
@@ -392,20 +358,25 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
             for (int r = 0; r < kBN / 128; ++r)                 // B: 512 B per 128 rows
               tmem_cp_32x128b_x4(sf_col + 4 + 4 * r, sd + ((kSfaBytes + 512u * r) >> 4));
           }
-          const uint64_t ad = adesc0 + ((stage * kABytes) >> 4);
-          const uint64_t bd = bdesc0 + ((stage * kBBytes) >> 4);
-          const uint32_t sfid = kBf16 ? 0u : static_cast<uint32_t>(kb & 3);
-          const uint32_t id = idesc0 | (sfid << 4) | (sfid << 29);
-          // four MMAs per k-block: K = 32 e4m3 or K = 16 bf16, 32 bytes each
-          // (+32 bytes along K = +2 in the descriptor's address field)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            if constexpr (kBf16)
-              mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, id,
-                       ((kb - kb_begin<kSplit>(p)) | k) != 0 ? 1u : 0u);
-            else
-              mma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, id, sf_col, sf_col + 4,
-                       ((kb - kb_begin<kSplit>(p)) | k) != 0 ? 1u : 0u);
+          for (int j = 0; j < kKps; ++j) {
+            if (j < n) {
+              const int kb = kbs + j;
+              const uint64_t ad = adesc0 + (((stage * kKps + j) * kABytes) >> 4);
+              const uint64_t bd = bdesc0 + (((stage * kKps + j) * kBBytes) >> 4);
+              const uint32_t sfid = kBf16 ? 0u : static_cast<uint32_t>(kb & 3);
+              const uint32_t id = idesc0 | (sfid << 4) | (sfid << 29);
+              // four MMAs per k-block: K = 32 e4m3 or K = 16 bf16, 32 bytes each
+              // (+32 bytes along K = +2 in the descriptor's address field)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                if constexpr (kBf16)
+                  mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, id, ((kb - kb0) | k) != 0 ? 1u : 0u);
+                else
+                  mma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, id, sf_col, sf_col + 4,
+                           ((kb - kb0) | k) != 0 ? 1u : 0u);
+              }
+            }
           }
           mma_commit(&empty[stage]);   // frees the stage's operands and scale-factor slot
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -477,10 +448,10 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
       uint32_t vcur[4] = {0u, 0u, 0u, 0u}, vnext[4] = {0u, 0u, 0u, 0u};
       if constexpr (!kFused) load_pack(kb0 / 4, vnext);   // fused A: the producers write SFA
       uint32_t bword[kRb];
-      for (int kb = kb0; kb < kb_end<kSplit>(p); ++kb) {
-        const bool pack_start = kb == kb0 || (kb & 3) == 0;
+      for (int kbs = kb0; kbs < kb_end<kSplit>(p); kbs += kKps) {
+        const bool pack_start = kbs == kb0 || (kbs & 3) == 0;
         if (pack_start) {   // a new pack: its words, and the next pack's load
-          const int j = kb / 4;
+          const int j = kbs / 4;
           if constexpr (!kFused) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) vcur[c] = vnext[c];
@@ -813,46 +784,18 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused>::kThreads, 1)
   }
 }
 
-// ----------------------------------------------------------- host side --
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return static_cast<EncodeTiledFn>(nullptr);
-    return reinterpret_cast<EncodeTiledFn>(ptr);
-  }();
-  return fn;
-}
-
-bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
-            const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,
-            CUtensorMapSwizzle swz) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint32_t elem_strides[3] = {1, 1, 1};
-  return fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides_bytes,
-            box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows, bool kFused = false>
+template <int kBN, int kEpi, int kSplit, bool kBf16, int kARows, bool kFused = false,
+          int kKps = 1>
 int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
   // q.after_own_kernel: the previous kernel on the stream does not write the
   // weights (inside dsv4_o_proj it is one of this library's), so the launch
   // may overlap it: this kernel reads only weights before griddep_wait().
-  using C = Cfg<kBN, kARows, kFused>;
+  using C = Cfg<kBN, kARows, kFused, kKps>;
   static std::atomic<int> configured_for[kMaxDevices];
   if (dev.device < 0 || dev.device >= kMaxDevices) return DSV4_ERR_UNSUPPORTED;
   const int configured = lazy_per_device(configured_for, dev.device, [] {
-    return cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows, kFused>,
+    return cudaFuncSetAttribute(block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows, kFused,
+                                                         kKps>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(C::smem_bytes)) == cudaSuccess ? 1 : 0;
   });
@@ -963,23 +906,25 @@ int launch_impl(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows, kFused>,
+  if (cudaLaunchKernelEx(&cfg,
+                         block_scaled_gemm_kernel<kBN, kEpi, kSplit, kBf16, kARows, kFused, kKps>,
                          tm_a, tm_b, tm_out, p) != cudaSuccess)
     return DSV4_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
-// The FP8 tile paths for one epilogue.
+// The FP8 tile paths for one epilogue: two k-blocks per stage (their k-ranges
+// start at 0 or, split over K, at a multiple of four k-blocks).
 template <int kEpi>
 int launch_fp8(const GemmProblem& q, bool wide, bool small_m, bool split, cudaStream_t stream,
                const DeviceInfo& dev) {
-  if (wide) return launch_impl<256, kEpi, 1, false, 128>(q, stream, dev);
+  if (wide) return launch_impl<256, kEpi, 1, false, 128, false, 1>(q, stream, dev);
   if (small_m) {
-    if (split) return launch_impl<128, kEpi, 2, false, 64>(q, stream, dev);
-    return launch_impl<128, kEpi, 1, false, 64>(q, stream, dev);
+    if (split) return launch_impl<128, kEpi, 2, false, 64, false, 2>(q, stream, dev);
+    return launch_impl<128, kEpi, 1, false, 64, false, 2>(q, stream, dev);
   }
-  if (split) return launch_impl<128, kEpi, 2, false, 128>(q, stream, dev);
-  return launch_impl<128, kEpi, 1, false, 128>(q, stream, dev);
+  if (split) return launch_impl<128, kEpi, 2, false, 128, false, 2>(q, stream, dev);
+  return launch_impl<128, kEpi, 1, false, 128, false, 2>(q, stream, dev);
 }
 
 }  // namespace
@@ -1002,6 +947,9 @@ int launch_block_scaled_gemm(const GemmProblem& q, cudaStream_t stream, const De
     if (quant) return launch_impl<128, kEpiQuant, 1, false, 64, true>(q, stream, dev);
     return launch_impl<128, kEpiBf16, 1, false, 64, true>(q, stream, dev);
   }
+  // Large FP8 shapes: 256 x 256 tiles on CTA pairs (two thirds of the
+  // shared-memory operand bytes per SM and k-block, three two-k-block stages)
+  if (pair_gemm_eligible(q, dev)) return launch_pair_gemm(q, stream, dev);
   // 256-wide tiles when they divide N and still give every SM a tile;
   // otherwise 128-wide tiles (twice the CTAs, for the small decode shapes)
   const int64_t m_tiles = (q.T + kBM - 1) / kBM;

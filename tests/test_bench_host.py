@@ -16,6 +16,10 @@ _KERNELS = {
     "quant": "void unnamed>::inv_rope_fp8_quant_kernel<4>(const unsigned short *)",
     "wo_a": "void unnamed>::block_scaled_gemm_kernel<256, 1, 1, 0, 128, 0>(CUtensorMap_st)",
     "wo_b": "void unnamed>::block_scaled_gemm_kernel<256, 0, 1, 0, 128, 0>(CUtensorMap_st)",
+    # the CTA-pair kernel of the large shapes: its only template argument is
+    # the epilogue (1: wo_a's re-quantisation)
+    "wo_a_pair": "void unnamed>::block_scaled_gemm_pair_kernel<1>(CUtensorMap_st)",
+    "wo_b_pair": "void unnamed>::block_scaled_gemm_pair_kernel<0>(CUtensorMap_st)",
 }
 
 
@@ -44,11 +48,23 @@ def test_summarize_traffic_groups_launches_by_kernel(tmp_path):
     path = tmp_path / "launches.csv"
     _write_launch_list(path, launches)
     lines = bench.summarize_traffic(str(path)).splitlines()
-    assert [l.split()[1] for l in lines[:3]] == list(bench.TRAFFIC_SOURCES)
+    n_src = len(bench.TRAFFIC_SOURCES)
+    assert [l.split()[1] for l in lines[:n_src]] == list(bench.TRAFFIC_SOURCES)
     body = [l.split() for l in lines if l.split()[0] in ("quant", "wo_a", "wo_b")]
     assert [b[0] for b in body] == ["quant", "quant", "wo_a", "wo_a", "wo_b", "wo_b"]
     assert body[0][1:] == ["538.0e6", "227.0e6", "128.7"]
     assert body[5][1:] == ["410.2e6", "48.0e6", "301.2"]
+
+
+def test_summarize_traffic_names_the_pair_kernels(tmp_path):
+    launches = [("wo_a_pair", 300_000_000, 50_000_000, 190_000),
+                ("wo_b_pair", 400_000_000, 48_000_000, 280_000)]
+    path = tmp_path / "launches.csv"
+    _write_launch_list(path, launches)
+    body = [l.split() for l in bench.summarize_traffic(str(path)).splitlines()
+            if l.split()[0] in ("quant", "wo_a", "wo_b")]
+    assert [b[0] for b in body] == ["wo_a", "wo_b"]
+    assert body[0][1:] == ["300.0e6", "50.0e6", "190.0"]
 
 
 def test_recorded_traffic_reads_the_committed_record_format(tmp_path, monkeypatch):
