@@ -7,6 +7,11 @@
 //
 //   C[t, g*N + n] = sum_k A[g][t][k] 2^ea[g][t][k/128] * B[g*N+n][k] 2^eb[(g*N+n)/128][k/128]
 //
+// This file holds the one-SM kernel, used for the shapes the CTA-pair kernel
+// (dsv4_gemm_pair.cu: 256 x 256 tiles on two SMs, the large FP8 shapes) does
+// not take: decode and mid sizes, the bf16 path, the quantiser-fused decode
+// kernel.  launch_block_scaled_gemm() below picks the kernel.
+//
 // Persistent, warp-specialised CTA, one per SM, tile 128 x kBN x 128 (kBN = 128
 // or 256, see Cfg):
 //   warp 0, lane 0   TMA producer: A tile (128 tokens x 128 k) and B tile
@@ -14,8 +19,8 @@
 //   warp 1, lane 0   MMA issuer: at the first k-block of each pack of four,
 //                    tcgen05.cp of the stage's scale factors into a TMEM
 //                    region; per k-block four tcgen05.mma (K = 32) from
-//                    precomputed descriptors, then one commit that frees the
-//                    stage.
+//                    precomputed descriptors; per stage (one or two k-blocks,
+//                    see Cfg) one commit that frees it.
 //   warp 2           scale-factor warp: each stage has its own scale-factor
 //                    slot, filled for the stage's k-block and completed on the
 //                    stage's full barrier (which therefore counts two
