@@ -443,31 +443,29 @@ def run_ours(args, ws, rank, local):
             stage_ms[j] += e[j].elapsed_time(e[j + 1])
     stage_ms = [x / n_ev for x in stage_ms]
 
-    # Up to 2048 tokens the library launches each GEMM to overlap the kernel
-    # before it, which per-kernel events would prevent: the step is timed
-    # again without them (same barrier / synchronize / max-over-ranks rules),
-    # and that is the reported value; the events above give the breakdown.
-    step_timing = "per-kernel events (the library overlaps no launches above 2048 tokens)"
-    if w.T <= 2048:
-        barrier()
+    # The library launches each GEMM to overlap the kernel before it, which
+    # per-kernel events would prevent: the step is timed again without them
+    # (same barrier / synchronize / max-over-ranks rules), and that is the
+    # reported value; the events above give the breakdown.
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            k.dsv4_o_proj(*args_dev, **kw)
+            launches += k.dsv4_last_launch_count()
+        t1.record(stream)
         torch.cuda.synchronize(dev)
-        with ClockSampler(local) as clk:
-            t0.record(stream)
-            for i in range(args.steps):
-                k.dsv4_o_proj(*args_dev, **kw)
-                launches += k.dsv4_last_launch_count()
-            t1.record(stream)
-            torch.cuda.synchronize(dev)
-        barrier()
-        ms_events = ms_total
-        ms_total = max_over_ranks(t0.elapsed_time(t1))
-        if k.dsv4_device_status(clear=True) != 0:
-            raise RuntimeError("device status error in the timed region")
-        ms_step = ms_total / args.steps
-        value = job_throughput(w.T, ws, args.steps, ms_total)
-        step_timing = (f"launches overlapped, no events (with per-kernel events: "
-                       f"{ms_events / args.steps:.4f} ms per step)")
-        launches //= 2
+    barrier()
+    ms_events = ms_total
+    ms_total = max_over_ranks(t0.elapsed_time(t1))
+    if k.dsv4_device_status(clear=True) != 0:
+        raise RuntimeError("device status error in the timed region")
+    ms_step = ms_total / args.steps
+    value = job_throughput(w.T, ws, args.steps, ms_total)
+    step_timing = (f"launches overlapped, no events (with per-kernel events: "
+                   f"{ms_events / args.steps:.4f} ms per step)")
+    launches //= 2
 
     # --- e2e: host buffers in, host result out, through the same C-ABI call.
     # Every step copies its own o and positions from pinned host memory and

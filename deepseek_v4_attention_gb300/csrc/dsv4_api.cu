@@ -425,11 +425,11 @@ int o_proj(const void* o, const int64_t* positions, const float* cos_sin_cache, 
   if (stage_events &&
       cudaEventRecord(static_cast<cudaEvent_t>(stage_events[1]), s) != cudaSuccess)
     return DSV4_ERR_CUDA;
-  // Programmatic launches overlap a GEMM's prologue and first weight loads with
-  // the previous kernel's tail: measured -2 % time at T <= 512 and +0.6 % at
-  // T = 4096, so only for small calls (and never when stage events are asked
-  // for, whose per-kernel times would then overlap).
-  const bool overlap = stage_events == nullptr && num_tokens <= 2048;
+  // Programmatic launches overlap a GEMM's prologue (and, on one SM, its first
+  // weight loads) with the previous kernel's tail: measured -2 % time at
+  // T <= 512, -1.0 % at T = 4096 and -1.4 % at T = 8192; never when stage
+  // events are asked for, whose per-kernel times would then overlap.
+  const bool overlap = stage_events == nullptr;
   rc = o_proj_gemms(w.x, w.xs, num_tokens, n_groups, D, o_lora_rank, hidden, wo_a_fp8,
                     wo_a_scale, wo_b_fp8, wo_b_scale, out, out_f32, w.zq, w.zs, overlap,
                     stage_events, s, dev);
