@@ -42,6 +42,25 @@ def test_grouped_wo_a_random_operands(dev, T, G, D, R):
     assert err <= GEMM_RTOL, err
 
 
+# Shapes of the CTA-pair kernel (more than 128 tokens, N % 256 == 0, at least
+# one 256 x 256 tile per two SMs: ceil(T/256) * N/256 * G >= 76 on 152 SMs):
+# the odd CTA's 128 rows all past T (T = 300) or holding one token (T = 129);
+# one k-block (a single one-k-block stage); three k-blocks (a stage of two,
+# then one); a dense GEMM whose last raster group has one 256-token block
+# (T = 2304: groups of 8 and 1 m-blocks).
+@pytest.mark.parametrize("T,G,D,R", [(300, 16, 512, 1024), (129, 16, 512, 2048),
+                                     (1200, 4, 128, 1024), (1200, 4, 384, 1024),
+                                     (2304, 1, 256, 2560)])
+def test_grouped_wo_a_pair_kernel_edges(dev, T, G, D, R):
+    assert -(-T // 256) * (R // 256) * G >= 76 and T > 128 and R % 256 == 0
+    T_al = oracle.tma_aligned_tokens(T)
+    x, xs = di.random_fp8_activation(T, G, D, seed=T * 3 + D, tma_aligned_T=T_al)
+    w, ws = di.fp8_block_weight(G * R, D, seed=T + 7 * D)
+    zg = _gpu_wo_a(x, xs, w, ws, T, G, D, R, dev)
+    _, z64 = oracle.grouped_gemm(x, xs, w, ws, T, G, D, R, want_fp64=True)
+    assert gemm_rel_err(zg, z64) <= GEMM_RTOL
+
+
 @pytest.mark.parametrize("T,G,D,R", [(130, 2, 512, 256), (1200, 16, 512, 256)])
 def test_grouped_wo_a_identity_weight_is_exact(dev, T, G, D, R):
     """W = I in every group with unit scales: z must equal bf16(dq_x) exactly."""
@@ -360,7 +379,9 @@ def test_fused_wo_a_out_of_range_position(dev):
     assert np.array_equal(zf, zs)
 
 
-@pytest.mark.parametrize("name,T", [("decode", 64), ("decode", 7), ("prefill", 300)])
+# ("full", 600): the CTA-pair kernel (3 x 4 x 16 pair tiles)
+@pytest.mark.parametrize("name,T", [("decode", 64), ("decode", 7), ("prefill", 300),
+                                    ("full", 600)])
 def test_grouped_wo_a_overlapping_the_quantiser(dev, name, T):
     """wo_a launched to overlap the kernel before it (DSV4_OVERLAP_PREVIOUS):
     the quantiser overwrites x with another token batch just before, on the
