@@ -297,9 +297,10 @@ def measured_peaks() -> tuple[dict, str]:
 
 
 # Dense tensor-core work per SM and clock of the MMAs the kernels issue
-# (tcgen05.mma, one CTA per SM): kind::mxf8f6f4 with e4m3 operands, 128 x 256
-# x 32 multiply-adds in 128 cycles = 16384 flop per clock; kind::f16 with bf16
-# operands half of that.  152 SMs at 1.81 GHz give the nominal 4.5 PFLOP/s FP8.
+# (tcgen05.mma): kind::mxf8f6f4 with e4m3 operands, 128 x 256 x 32
+# multiply-adds per SM in 128 cycles (one SM's tile, or its half of a CTA
+# pair's 256 x 256 x 32) = 16384 flop per clock; kind::f16 with bf16 operands
+# half of that.  152 SMs at 1.81 GHz give the nominal 4.5 PFLOP/s FP8.
 MMA_FLOP_PER_CLK_SM = {"e4m3": 16384.0, "bf16": 8192.0}
 SUSTAINED_REGION_S = 1.0   # timed regions at least this long use the sustained peak
 

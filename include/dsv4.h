@@ -119,10 +119,12 @@ int dsv4_grouped_wo_a(const void* x_fp8, const int32_t* x_scale, int64_t num_tok
  *
  * DSV4_OVERLAP_PREVIOUS: the kernel is launched with programmatic stream
  * serialization, so that it starts while the previous kernel on `stream`
- * still runs: its prologue and its reads of w_fp8 and w_scale (the first
- * pipeline stages into shared memory, the rest of each CTA's first weight
- * tile into L2) overlap that kernel, and every read of x_fp8 / x_scale and
- * every write of z waits until that kernel has completed.  For the
+ * still runs: its prologue and, for the shapes served by one CTA per tile
+ * (the large FP8 shapes run on CTA pairs, which wait before any read), its
+ * reads of w_fp8 and w_scale (the first pipeline stages into shared memory,
+ * the rest of each CTA's first weight tile into L2) overlap that kernel, and
+ * every read of x_fp8 / x_scale and every write of z waits until that kernel
+ * has completed.  For the
  * weight-read-bound decode shapes this hides the launch and much of the
  * weight stream behind the kernel before (in a decode step, the quantiser).
  * The caller guarantees that the previous kernel on the stream does not write
