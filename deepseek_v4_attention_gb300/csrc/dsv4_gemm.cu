@@ -114,7 +114,10 @@ struct Cfg {
   static constexpr uint32_t ostage = (sf + kSfSlots * kSfSlotBytes + 1023) / 1024 * 1024;
   // per epilogue warp, a 2 KiB staging buffer for its TMA stores (32 rows x 64 B)
   static constexpr uint32_t kEpiBufBytes = 2048;
-  static constexpr uint32_t epi = ostage + kOStages * kOBytes;
+  // fused A: each token row's cos || sin cache row (64 fp32), copied per tile
+  static constexpr uint32_t kCsBytes = kFused ? kARows * 256 : 0;
+  static constexpr uint32_t csrows = ostage + kOStages * kOBytes;
+  static constexpr uint32_t epi = csrows + kCsBytes;
   static constexpr uint32_t bars = epi + kEpiWarps * kEpiBufBytes;
   // full/empty[kStages], tmem_full/empty[kAccBufs], drain, o_full/o_empty[kOStages]
   static constexpr uint32_t n_bars = 2 * kStages + 2 * kAccBufs + 1 + 2 * kOStages;
@@ -501,8 +504,10 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused, kKps>::kThreads, 1)
     // the stage's scale-factor slot.  The k-block's bf16 slice arrives by TMA
     // in the o ring; a half-warp owns one token row (lane l16 holds its
     // elements 8 l16 .. 8 l16 + 7, 16 contiguous bytes of the row's 256);
-    // warp pw owns rows 16 pw .. 16 pw + 15, two per step.  The cos/sin
-    // values of a row's rope lanes are loaded once per tile.
+    // warp pw owns rows 16 pw .. 16 pw + 15, two per step.  Each row's
+    // cos || sin cache row is copied into shared memory once per tile and
+    // read at the rope block of each head (held in registers for all rows,
+    // the values spilled and the warp took ~3000 cycles per k-block).
     constexpr int kSteps = kARows / (2 * (C::kProdWarps > 0 ? C::kProdWarps : 1));
     const int pw = warp - C::kProdWarp0;
     const int half = lane >> 4;
@@ -518,29 +523,28 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused, kKps>::kThreads, 1)
       tile_coords(p, tile, g, n_blk, m_blk);
       const int64_t m0 = static_cast<int64_t>(m_blk) * kBM;
       // each row's position; one outside [0, max_pos) is recorded and leaves
-      // the row unrotated, as in the quantiser
-      bool rot[kSteps];
-      float4 cs[kSteps], sn[kSteps];
+      // the row unrotated, as in the quantiser.  Lane l16 copies float4 l16
+      // of the row's cache row (cos: 0..7, sin: 8..15).
+      float4* cs_rows = reinterpret_cast<float4*>(smem + C::csrows);   // [kARows][16]
+      uint32_t rot_mask = 0;
+      __syncwarp();   // the previous tile's reads of this warp's rows are done
 #pragma unroll
       for (int st = 0; st < kSteps; ++st) {
-        const int64_t t = m0 + 16 * pw + 2 * st + half;
-        rot[st] = false;
-        cs[st] = make_float4(0.f, 0.f, 0.f, 0.f);
-        sn[st] = cs[st];
+        const int r = 16 * pw + 2 * st + half;
+        const int64_t t = m0 + r;
+        float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
         if (t < p.T) {
           const int64_t pos = __ldg(p.positions + t);
           if (pos >= 0 && pos < p.max_pos) {
-            rot[st] = true;
-            if (rope_lane) {
-              const float4* row = reinterpret_cast<const float4*>(p.cache + pos * 64);
-              cs[st] = __ldg(row + quad);
-              sn[st] = __ldg(row + 8 + quad);
-            }
+            rot_mask |= 1u << st;
+            cv = __ldg(reinterpret_cast<const float4*>(p.cache + pos * 64) + l16);
           } else if (l16 == 0) {
             record_status(p.status, DSV4_ERR_RANGE);
           }
         }
+        cs_rows[r * 16 + l16] = cv;
       }
+      __syncwarp();
       for (int kb = kb_begin<kSplit>(p); kb < kb_end<kSplit>(p); ++kb) {
         const int qb = kb & 3;
         if (!mbar_wait_warp(&o_full[oj], ophase, abort_flag, p.status)) { ok = false; break; }
@@ -560,11 +564,14 @@ __global__ void __launch_bounds__(Cfg<kBN, kARows, kFused, kKps>::kThreads, 1)
         // the cast instead of being held.
         auto values = [&](int st, float (&f)[8]) {
           unpack8(v[st], f);
-          if (qb == 3 && rope_lane && rot[st]) {
-            inv_rotate(f[0], f[1], cs[st].x, sn[st].x);
-            inv_rotate(f[2], f[3], cs[st].y, sn[st].y);
-            inv_rotate(f[4], f[5], cs[st].z, sn[st].z);
-            inv_rotate(f[6], f[7], cs[st].w, sn[st].w);
+          if (qb == 3 && rope_lane && ((rot_mask >> st) & 1u)) {
+            const int r = 16 * pw + 2 * st + half;
+            const float4 c = cs_rows[r * 16 + quad];
+            const float4 sn = cs_rows[r * 16 + 8 + quad];
+            inv_rotate(f[0], f[1], c.x, sn.x);
+            inv_rotate(f[2], f[3], c.y, sn.y);
+            inv_rotate(f[4], f[5], c.z, sn.z);
+            inv_rotate(f[6], f[7], c.w, sn.w);
           }
         };
         float m[kSteps];
