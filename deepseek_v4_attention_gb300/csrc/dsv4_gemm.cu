@@ -959,8 +959,9 @@ int launch_block_scaled_gemm(const GemmProblem& q, cudaStream_t stream, const De
     if (quant) return launch_impl<128, kEpiQuant, 1, false, 64, true>(q, stream, dev);
     return launch_impl<128, kEpiBf16, 1, false, 64, true>(q, stream, dev);
   }
-  // Large FP8 shapes: 256 x 256 tiles on CTA pairs (two thirds of the
-  // shared-memory operand bytes per SM and k-block, three two-k-block stages)
+  // Large shapes (FP8, and bf16 with the bf16 epilogue): 256 x 256 tiles on CTA
+  // pairs (two thirds of the shared-memory operand bytes per SM and k-block,
+  // three two-k-block stages)
   if (pair_gemm_eligible(q, dev)) return launch_pair_gemm(q, stream, dev);
   // 256-wide tiles when they divide N and still give every SM a tile;
   // otherwise 128-wide tiles (twice the CTAs, for the small decode shapes)

@@ -1,6 +1,7 @@
 // dsv4_gemm_pair.cu -- the block-scaled FP8 GEMM on CTA pairs
 // (tcgen05.mma.cta_group::2), for the large shapes of both projections (the
-// grouped wo_a with its fused z re-quantisation, the dense wo_b):
+// grouped wo_a with its fused z re-quantisation, the dense wo_b), and its
+// bf16 form (kBf16: kind::f16, no scale factors) for the non-FP8 grouped wo_a:
 //
 //   C[t, g*N + n] = sum_k A[g][t][k] 2^ea[g][t][k/128] * B[g*N+n][k] 2^eb[(g*N+n)/128][k/128]
 //
@@ -76,6 +77,16 @@ __device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, 
       "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
       " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -193,14 +204,18 @@ struct PairCfg {
   static constexpr uint32_t smem_bytes = total + 1024;   // + alignment slack
 };
 
-template <int kEpi>
+// kBf16: A and B bf16 (a k-block is 64 elements, still 128 bytes a row),
+// tcgen05.mma.kind::f16 without scale factors, bf16 output only.
+template <int kEpi, bool kBf16>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     block_scaled_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a,
                                   const __grid_constant__ CUtensorMap tm_b,
                                   const __grid_constant__ CUtensorMap tm_out, const Params p) {
   using C = PairCfg;
+  static_assert(!kBf16 || kEpi == kEpiBf16, "the bf16 GEMM has the bf16 epilogue only");
   constexpr int kStages = C::kStages;
   constexpr int kKps = C::kKps;
+  constexpr int kBKe = kBf16 ? 64 : kBK;   // elements of K per 128-byte k-block
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -224,7 +239,8 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 2);            // the producer's expect_tx, the scale-factor warp
+      // the producer's expect_tx and (FP8) the scale-factor warp
+      mbar_init(&full[s], kBf16 ? 1 : 2);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
@@ -269,12 +285,12 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
           if (leader)
             mbar_arrive_expect_tx(&full[stage],
                                   2u * static_cast<uint32_t>(n) * (C::kABytes + C::kBBytes) +
-                                      ((kbs & 3) == 0 ? 16u : 0u));
+                                      ((!kBf16 && (kbs & 3) == 0) ? 16u : 0u));
           const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(stage);
           for (int j = 0; j < n; ++j) {
             const int slot = stage * kKps + j;
-            tma_load_3d_pair(smem + C::a + slot * C::kABytes, &tm_a, fb, (kbs + j) * kBK, m0, g);
-            tma_load_2d_pair(smem + C::b + slot * C::kBBytes, &tm_b, fb, (kbs + j) * kBK, brow);
+            tma_load_3d_pair(smem + C::a + slot * C::kABytes, &tm_a, fb, (kbs + j) * kBKe, m0, g);
+            tma_load_2d_pair(smem + C::b + slot * C::kBBytes, &tm_b, fb, (kbs + j) * kBKe, brow);
           }
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -294,7 +310,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       const uint64_t adesc0 = smem_desc(smem_addr(smem + C::a), 16, 1024, 2);
       const uint64_t bdesc0 = smem_desc(smem_addr(smem + C::b), 16, 1024, 2);
       const uint64_t sfdesc0 = smem_desc(smem_addr(smem + C::sf), 0, 128, 0);
-      const uint32_t idesc0 = mxf8_idesc(kPairM, C::kBN, 0, 0);
+      const uint32_t idesc0 = kBf16 ? bf16_idesc(kPairM, C::kBN) : mxf8_idesc(kPairM, C::kBN, 0, 0);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
@@ -316,7 +332,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
           // both CTAs' operands, both scale-factor slots at a pack start
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          if ((kbs & 3) == 0) {
+          if (!kBf16 && (kbs & 3) == 0) {
             sf_region = (sf_region + 1 == kStages) ? 0 : sf_region + 1;
             sf_col = tmem_base + static_cast<uint32_t>(C::kSfCol0 + sf_region * C::kSfColsPerSlot);
             const uint64_t sd = sfdesc0 + ((stage * C::kSfSlotBytes) >> 4);
@@ -332,12 +348,17 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
               const int slot = stage * kKps + j;
               const uint64_t ad = adesc0 + ((slot * C::kABytes) >> 4);
               const uint64_t bd = bdesc0 + ((slot * C::kBBytes) >> 4);
-              const uint32_t sfid = static_cast<uint32_t>(kb & 3);
+              const uint32_t sfid = kBf16 ? 0u : static_cast<uint32_t>(kb & 3);
               const uint32_t id = idesc0 | (sfid << 4) | (sfid << 29);
+              // four MMAs per k-block: K = 32 e4m3 or K = 16 bf16, 32 bytes each
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_mxf8_pair(tmem_base, ad + 2 * k, bd + 2 * k, id, sf_col, sf_col + 4,
-                              (kb | k) != 0 ? 1u : 0u);
+              for (int k = 0; k < 4; ++k) {
+                if constexpr (kBf16)
+                  mma_bf16_pair(tmem_base, ad + 2 * k, bd + 2 * k, id, (kb | k) != 0 ? 1u : 0u);
+                else
+                  mma_mxf8_pair(tmem_base, ad + 2 * k, bd + 2 * k, id, sf_col, sf_col + 4,
+                                (kb | k) != 0 ? 1u : 0u);
+              }
             }
           }
           mma_commit_both(&empty[stage]);   // frees the stage in both CTAs
@@ -353,7 +374,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         mbar_wait_drain(drain, 0);
       }
     }
-  } else if (warp == 2) {
+  } else if (warp == 2 && !kBf16) {
     // ------------------------------------------------------ scale factors
     constexpr int kRb = C::kBN / 128;   // 128-column weight-scale blocks per tile
     const int packs = p.packs;
@@ -426,7 +447,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       while (global_timer_ns() - t0 < 1000000ull) {
       }
     }
-  } else {
+  } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
     const int epi = warp - C::kEpiWarp0;  // 0 .. 7
     const int quarter = warp & 3;         // TMEM lanes this warp may access
@@ -563,38 +584,42 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   }
 }
 
-template <int kEpi>
+template <int kEpi, bool kBf16 = false>
 int launch_pair(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
   using C = PairCfg;
   static std::atomic<int> configured_for[kMaxDevices];
   if (dev.device < 0 || dev.device >= kMaxDevices) return DSV4_ERR_UNSUPPORTED;
   const int configured = lazy_per_device(configured_for, dev.device, [] {
-    return cudaFuncSetAttribute(block_scaled_gemm_pair_kernel<kEpi>,
+    return cudaFuncSetAttribute(block_scaled_gemm_pair_kernel<kEpi, kBf16>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(C::smem_bytes)) == cudaSuccess ? 1 : 0;
   });
   if (!configured) return DSV4_ERR_CUDA;
   const int64_t T = q.T;
   const int64_t t_al = (T + 3) / 4 * 4;
+  // operands: 128-byte rows of K per k-block (128 e4m3 or 64 bf16 elements)
+  const int esz = kBf16 ? 2 : 1;
+  const int kbe = kBK / esz;
+  const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUtensorMap tm_a, tm_b, tm_out;
   {
-    // A: [G][T][K] e4m3; a box is this CTA's 128 token rows x one 128-byte k-block
+    // A: [G][T][K]; a box is this CTA's 128 token rows x one 128-byte k-block
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(q.K), static_cast<cuuint64_t>(T),
                           static_cast<cuuint64_t>(q.G)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.K), static_cast<cuuint64_t>(T * q.K)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM), 1};
-    if (!encode(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q.a, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_128B))
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(q.K) * esz,
+                             static_cast<cuuint64_t>(T * q.K) * esz};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kbe), static_cast<cuuint32_t>(kBM), 1};
+    if (!encode(&tm_a, dt, 3, q.a, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return DSV4_ERR_CUDA;
   }
   {
-    // B: [G*N][K] e4m3; a box is this CTA's 128 output columns x one k-block
+    // B: [G*N][K]; a box is this CTA's 128 output columns x one k-block
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(q.K),
                           static_cast<cuuint64_t>(static_cast<int64_t>(q.G) * q.N)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(q.K)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(C::kBN / 2)};
-    if (!encode(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q.b, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_128B))
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(q.K) * esz};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kbe), static_cast<cuuint32_t>(C::kBN / 2)};
+    if (!encode(&tm_b, dt, 2, q.b, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return DSV4_ERR_CUDA;
   }
   {
@@ -621,7 +646,7 @@ int launch_pair(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   p.m_tiles = static_cast<int>((T + kPairM - 1) / kPairM);   // 256-token blocks
   p.n_tiles = q.N / C::kBN;
   p.num_tiles = p.m_tiles * p.n_tiles * q.G;
-  p.k_blocks = q.K / kBK;
+  p.k_blocks = q.K / kbe;
   p.packs = (q.K / 128 + 3) / 4;
   p.t_al = t_al;
   p.a_scale = q.a_scale;
@@ -655,7 +680,7 @@ int launch_pair(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
     c.attrs = attr;
     c.numAttrs = 1;
     int n = 0;
-    return cudaOccupancyMaxActiveClusters(&n, block_scaled_gemm_pair_kernel<kEpi>, &c) ==
+    return cudaOccupancyMaxActiveClusters(&n, block_scaled_gemm_pair_kernel<kEpi, kBf16>, &c) ==
                    cudaSuccess ? n : 0;
   });
   if (max_pairs <= 0) return DSV4_ERR_CUDA;
@@ -668,7 +693,7 @@ int launch_pair(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_pair_kernel<kEpi>, tm_a, tm_b, tm_out, p) !=
+  if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_pair_kernel<kEpi, kBf16>, tm_a, tm_b, tm_out, p) !=
       cudaSuccess)
     return DSV4_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
@@ -677,13 +702,18 @@ int launch_pair(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev
 }  // namespace
 
 bool pair_gemm_eligible(const GemmProblem& q, const DeviceInfo& dev) {
-  if (q.bf16 || q.fused_a || q.N % PairCfg::kBN != 0 || q.K % kBK != 0) return false;
-  if (q.K / 128 > 4 * 32 * 4) return false;   // weight-scale words held per lane
+  if (q.fused_a || q.N % PairCfg::kBN != 0) return false;
+  if (q.bf16) {
+    if (q.K % 64 != 0 || q.epilogue != kEpiBf16) return false;
+  } else {
+    if (q.K % kBK != 0 || q.K / 128 > 4 * 32 * 4) return false;   // weight-scale words per lane
+  }
   const int64_t pair_tiles = (q.T + kPairM - 1) / kPairM * (q.N / PairCfg::kBN) * q.G;
   return q.T > kBM && pair_tiles >= dev.num_sms / 2;
 }
 
 int launch_pair_gemm(const GemmProblem& q, cudaStream_t stream, const DeviceInfo& dev) {
+  if (q.bf16) return launch_pair<kEpiBf16, true>(q, stream, dev);
   switch (q.epilogue) {
     case kEpiQuant: return launch_pair<kEpiQuant>(q, stream, dev);
     case kEpiF32: return launch_pair<kEpiF32>(q, stream, dev);

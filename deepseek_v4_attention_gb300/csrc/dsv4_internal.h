@@ -96,8 +96,9 @@ int launch_inv_rope_bf16(const void* o, const int64_t* positions, const float* c
 int launch_block_scaled_gemm(const GemmProblem& p, cudaStream_t stream, const DeviceInfo& dev);
 
 // The CTA-pair GEMM (dsv4_gemm_pair.cu): 256 x 256 tiles on two SMs, for the
-// large FP8 shapes; eligible: FP8 A from memory, N % 256 == 0, more than 128
-// tokens and at least one pair tile per two SMs.
+// large shapes; eligible: A from memory (FP8, or bf16 with the bf16
+// epilogue), N % 256 == 0, more than 128 tokens and at least one pair tile
+// per two SMs.
 bool pair_gemm_eligible(const GemmProblem& p, const DeviceInfo& dev);
 int launch_pair_gemm(const GemmProblem& p, cudaStream_t stream, const DeviceInfo& dev);
 

@@ -28,10 +28,12 @@ def _gpu_wo_a(x, xs, w, ws, T, G, D, R, dev):
     return to_bits(z)
 
 
-# the last case takes the 256-wide tile path (>= one tile per SM), the others 128-wide
+# (1200, 4, 640, 1024) runs on CTA pairs (5 x 4 x 4 pair tiles); (128, 16, 256,
+# 2560) on one SM with 256-wide tiles (T <= 128: no pairs; 10 x 16 tiles >= one
+# per SM); the others on one SM with 128-wide tiles
 @pytest.mark.parametrize("T,G,D,R", [(16, 2, 1024, 128), (64, 8, 4096, 1024), (1, 1, 128, 128),
                                      (3, 2, 512, 256), (129, 3, 640, 384), (200, 1, 1024, 896),
-                                     (1200, 4, 640, 1024)])
+                                     (1200, 4, 640, 1024), (128, 16, 256, 2560)])
 def test_grouped_wo_a_random_operands(dev, T, G, D, R):
     T_al = oracle.tma_aligned_tokens(T)
     x, xs = di.random_fp8_activation(T, G, D, seed=T * 7 + G, tma_aligned_T=T_al)
@@ -273,8 +275,13 @@ def test_inv_rope_bf16_parity(dev, name, T):
     assert np.array_equal(got, ref)          # same fp32 order, same rounding: bit-exact
 
 
+# CTA pairs: (1200, 4, 512, 1024) (8 k-blocks of 64), (300, 16, 192, 1024)
+# (three k-blocks; the odd CTA's rows past T), (129, 16, 64, 2048) (one k-block,
+# one token in the odd CTA); one SM, 256-wide: (128, 16, 256, 2560)
 @pytest.mark.parametrize("T,G,D,R", [(16, 2, 1024, 128), (64, 8, 4096, 1024), (3, 1, 64, 128),
-                                     (129, 3, 640, 384), (1200, 4, 512, 1024)])
+                                     (129, 3, 640, 384), (1200, 4, 512, 1024),
+                                     (300, 16, 192, 1024), (129, 16, 64, 2048),
+                                     (128, 16, 256, 2560)])
 def test_grouped_wo_a_bf16_parity(dev, T, G, D, R):
     import deepseek_v4_attention_gb300 as k
     rng = np.random.default_rng(T + G)
