@@ -271,7 +271,8 @@ def summarize_traffic(csv_path: str) -> str:
             return "quant"
         # the re-quantising epilogue (kEpi = 1) is wo_a's: the first template
         # argument of the CTA-pair kernel, the second of the one-SM kernel
-        return "wo_a" if ("pair_kernel<1>" in name or "<256, 1," in name) else "wo_b"
+        pair_quant = "pair_kernel<1>" in name or "pair_kernel<1," in name
+        return "wo_a" if (pair_quant or "<256, 1," in name) else "wo_b"
 
     csrc = os.path.join(ROOT, "deepseek_v4_attention_gb300", "csrc")
     lines = []

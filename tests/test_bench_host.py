@@ -16,10 +16,10 @@ _KERNELS = {
     "quant": "void unnamed>::inv_rope_fp8_quant_kernel<4>(const unsigned short *)",
     "wo_a": "void unnamed>::block_scaled_gemm_kernel<256, 1, 1, 0, 128, 0>(CUtensorMap_st)",
     "wo_b": "void unnamed>::block_scaled_gemm_kernel<256, 0, 1, 0, 128, 0>(CUtensorMap_st)",
-    # the CTA-pair kernel of the large shapes: its only template argument is
-    # the epilogue (1: wo_a's re-quantisation)
-    "wo_a_pair": "void unnamed>::block_scaled_gemm_pair_kernel<1>(CUtensorMap_st)",
-    "wo_b_pair": "void unnamed>::block_scaled_gemm_pair_kernel<0>(CUtensorMap_st)",
+    # the CTA-pair kernel of the large shapes: its first template argument is
+    # the epilogue (1: wo_a's re-quantisation), the second whether it is bf16
+    "wo_a_pair": "void unnamed>::block_scaled_gemm_pair_kernel<1, 0>(CUtensorMap_st)",
+    "wo_b_pair": "void unnamed>::block_scaled_gemm_pair_kernel<0, 0>(CUtensorMap_st)",
 }
 
 
