@@ -8,7 +8,7 @@
 // A cluster of two CTAs (on two SMs) computes a 256-token x 256-column tile.
 // Each CTA stages its own 128 token rows of A and its own 128 of the tile's
 // B rows (output columns); one thread of the even CTA issues
-// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 32), which reads both CTAs'
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 32; K = 16 bf16), which reads both CTAs'
 // shared memory and leaves in each CTA's tensor memory the 128 x 256 fp32
 // accumulator of its own tokens.  Per SM and 128-deep k-block the operands are
 // 32 KiB (48 KiB for a 128 x 256 tile on one SM), so the same shared memory
@@ -26,7 +26,7 @@
 //                    of four, tcgen05.cp of the stage's scale factors into a
 //                    TMEM region of both CTAs; per k-block four MMAs, per
 //                    stage one commit that frees it in both CTAs (multicast).
-//   warp 2           scale factors: at the first k-block of a pack each CTA
+//   warp 2           (FP8) scale factors: at the first k-block of a pack each CTA
 //                    writes the 128 A scale words of its own tokens and the B
 //                    scales of all 256 columns into the stage's slot of its own
 //                    shared memory.  The even CTA's warp then arrives on the
@@ -36,8 +36,10 @@
 //                    barrier (an arrive at cluster scope costs ~2000 cycles, a
 //                    bulk copy's completion rides the TMA path).
 //   warps 3..10      epilogue: the CTA's 128 x 256 accumulator to registers
-//                    (each warp 32 rows x 128 columns), a release of the
-//                    accumulator to the even CTA's MMA thread, then the bf16 /
+//                    (each warp 32 rows x 128 columns, one tcgen05.ld), a
+//                    release of the accumulator to the even CTA's MMA thread
+//                    (the odd CTA's warps: a relaxed cluster-scope arrive on
+//                    the even CTA's barrier), then the bf16 /
 //                    fp32 store or the per-128 FP8 re-quantisation, through a
 //                    swizzled staging buffer and TMA stores.
 // Every wait is bounded (the library's 2 s limit); a timeout records
