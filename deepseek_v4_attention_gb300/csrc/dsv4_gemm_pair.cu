@@ -38,8 +38,9 @@
 //   warps 3..10      epilogue: the CTA's 128 x 256 accumulator to registers
 //                    (each warp 32 rows x 128 columns, one tcgen05.ld), a
 //                    release of the accumulator to the even CTA's MMA thread
-//                    (the odd CTA's warps: a relaxed cluster-scope arrive on
-//                    the even CTA's barrier), then the bf16 /
+//                    (the odd CTA's warps: a 16-byte bulk copy into the even
+//                    CTA's shared memory, counted as transaction bytes on its
+//                    barrier), then the bf16 /
 //                    fp32 store or the per-128 FP8 re-quantisation, through a
 //                    swizzled staging buffer and TMA stores.
 // Every wait is bounded (the library's 2 s limit); a timeout records
@@ -140,16 +141,6 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// Arrive on an mbarrier of the other CTA of the pair (shared::cluster
-// address) without release semantics: used where the arrival publishes no
-// memory writes, only that this thread's tcgen05 loads have completed
-// (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync).  A release at
-// cluster scope measured ~2000 cycles per arrive.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-               : "memory");
-}
-
 // Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory into
 // another CTA's (dst_cluster, a shared::cluster address); its completion is
 // counted as transaction bytes on that CTA's mbarrier bar_cluster.
@@ -202,7 +193,9 @@ struct PairCfg {
   static constexpr uint32_t misc = bars + n_bars * 8;    // tmem base, abort flag
   // 16 bytes per stage that the odd CTA's slot signal lands on (even CTA)
   static constexpr uint32_t sig = (misc + 16 + 15) / 16 * 16;
-  static constexpr uint32_t total = sig + 16 * kStages;
+  // 16 bytes per epilogue warp that the odd CTA's accumulator release lands on
+  static constexpr uint32_t esig = sig + 16 * kStages;
+  static constexpr uint32_t total = esig + 16 * kEpiWarps;
   static constexpr uint32_t smem_bytes = total + 1024;   // + alignment slack
 };
 
@@ -246,7 +239,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 2 * C::kEpiWarps);
+    mbar_init(tmem_empty, C::kEpiWarps);   // the even CTA's warps; the odd's by transaction bytes
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -456,6 +449,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     const int col_half = epi >> 2;        // which 128 columns of the tile
     const int row = quarter * 32 + lane;
     const uint32_t tmem_empty_leader = map_to_cta(smem_addr(tmem_empty), 0);
+    const uint32_t esig_leader = map_to_cta(smem_addr(smem + C::esig), 0);
     uint32_t acc_phase = 0;
     for (int tile = pair0; tile < p.num_tiles; tile += npairs) {
       int g, n_blk, m_blk;
@@ -475,9 +469,21 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {   // the accumulator may be overwritten once all 16 warps are here
-        if (leader) mbar_arrive(tmem_empty);
-        else mbar_arrive_remote_relaxed(tmem_empty_leader);
+      // The accumulator may be overwritten once all 16 warps have read it: the
+      // even CTA's eight arrive (its warp 0 expecting the odd CTA's 8 x 16
+      // bytes), the odd CTA's send 16 bytes each into the even CTA's shared
+      // memory, completing on the same barrier.  Nothing is sent after the
+      // pair's last tile (no MMA waits for it; no copy may be in flight when
+      // the CTAs exit).
+      if (lane == 0) {
+        const bool more = tile + npairs < p.num_tiles;
+        if (leader) {
+          if (epi == 0 && more) mbar_arrive_expect_tx(tmem_empty, 16u * C::kEpiWarps);
+          else mbar_arrive(tmem_empty);
+        } else if (more) {
+          bulk_copy_to_cta(esig_leader + 16u * static_cast<uint32_t>(epi),
+                           smem + C::esig + 16 * epi, 16u, tmem_empty_leader);
+        }
       }
       // Stores through this warp's staging buffer: each lane writes its row's
       // 64-byte chunk with the 64-byte TMA swizzle (16-byte unit q of row r at
@@ -571,6 +577,14 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       }
     }
     if (lane == 0) bulk_wait_all();   // every store complete before the CTA leaves
+    __syncwarp();
+    if (!leader && *abort_flag && lane == 0) {
+      // a release signal in flight completes on the even CTA's barrier: give
+      // it time to land (both CTAs stay resident until the final barrier)
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 1000000ull) {
+      }
+    }
     __syncwarp();
   }
 
