@@ -527,16 +527,21 @@ def run_ours(args, ws, rank, local):
             e.record(stream)
         run(2)
         torch.cuda.synchronize(dev)
-        barrier()
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        run(e2e_steps)
-        stream.wait_stream(s_out)                       # the last read-back is inside
-        a1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
-        e_ms = max_over_ranks(a0.elapsed_time(a1))
+        # three timed regions, the median reported (a stall of the host side
+        # of the pipeline in one region was seen once in nine runs)
+        e_runs = []
+        for _ in range(3):
+            barrier()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            run(e2e_steps)
+            stream.wait_stream(s_out)                   # the last read-back is inside
+            a1.record(stream)
+            torch.cuda.synchronize(dev)
+            barrier()
+            e_runs.append(max_over_ranks(a0.elapsed_time(a1)))
+        e_ms = statistics.median(e_runs)
         h2d_bytes = o_h[0].numel() * 2 + p_h[0].numel() * 8
         d2h_bytes = out_h[0].numel() * 2
         # the host link measured on this machine in this run: one copy of the
@@ -549,7 +554,8 @@ def run_ours(args, ws, rank, local):
         bound = job_throughput(w.T, ws, 1, bound_ms)
         e2e = {"value": value_e2e, "unit": UNIT,
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
-               "steps": e2e_steps,
+               "steps": e2e_steps, "regions": 3,
+               "region_values": [job_throughput(w.T, ws, e2e_steps, x) for x in e_runs],
                "pipeline": "input copy / compute / read-back of consecutive steps overlap "
                            "(two buffers, three streams)",
                "link": {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
