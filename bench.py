@@ -764,7 +764,7 @@ def _graph_ms(fn, steps: int, stream) -> dict:
 CONFIG_WORKLOADS = ("tiny", "decode", "prefill", "quant1k", "quant8k", "quant32k")
 
 
-def run_workload(name: str, steps: int, warmup: int, local: int) -> dict:
+def run_workload(name: str, steps: int, warmup: int, local: int, tokens: int | None = None) -> dict:
     """One of the smaller synthetic workloads: quant (+ grouped wo_a).  Each step
     uses the next of several rotating input sets whose total exceeds 3x L2, so
     that weights and activations come from HBM, not from the previous step.
@@ -776,6 +776,8 @@ def run_workload(name: str, steps: int, warmup: int, local: int) -> dict:
     torch.cuda.set_device(dev)
     bf16 = name.endswith("_bf16")
     w = di.WORKLOADS[name.replace("_bf16", "")]
+    if tokens:                 # the same shapes at another token count
+        w = w.with_tokens(tokens)
     gemm = not w.name.startswith("quant")
     on_device = w.name in ("quant8k", "quant32k")
     host = di.make_inputs(w, with_wo_b=False, o_device=dev if on_device else None)
@@ -939,7 +941,7 @@ def main():
     elif args.workload != "full":
         if ws > 1:
             raise SystemExit("--workload other than full runs on one GPU")
-        res = run_workload(args.workload, args.steps, args.warmup, local)
+        res = run_workload(args.workload, args.steps, args.warmup, local, args.tokens)
     else:
         res = run_ours(args, ws, rank, local)
     if rank == 0 and res is not None:
