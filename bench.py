@@ -527,10 +527,10 @@ def run_ours(args, ws, rank, local):
             e.record(stream)
         run(2)
         torch.cuda.synchronize(dev)
-        # three timed regions, the median reported (a stall of the host side
-        # of the pipeline in one region was seen once in nine runs)
+        # five timed regions, the median reported (stalls of the host side of
+        # the pipeline have hit single regions)
         e_runs = []
-        for _ in range(3):
+        for _ in range(5):
             barrier()
             a0 = torch.cuda.Event(enable_timing=True)
             a1 = torch.cuda.Event(enable_timing=True)
@@ -554,7 +554,7 @@ def run_ours(args, ws, rank, local):
         bound = job_throughput(w.T, ws, 1, bound_ms)
         e2e = {"value": value_e2e, "unit": UNIT,
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
-               "steps": e2e_steps, "regions": 3,
+               "steps": e2e_steps, "regions": 5,
                "region_values": [job_throughput(w.T, ws, e2e_steps, x) for x in e_runs],
                "pipeline": "input copy / compute / read-back of consecutive steps overlap "
                            "(two buffers, three streams)",
